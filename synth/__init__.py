@@ -1,0 +1,195 @@
+"""Seeded synthetic inputs for the GEMM workloads.
+
+This module only draws random numbers and rounds them once to the storage
+type (fp16 / bf16 with round-to-nearest-even, int4 packed two per byte).  It
+holds none of the GEMM arithmetic, so both the CUDA path and the CPU oracle
+can consume its output without sharing any of the method's code.
+
+Every array is returned as raw storage bits in numpy (uint16 for 16-bit
+floats, uint8 for packed int4, float32 for fp32), laid out exactly as the
+library expects them:
+
+* A   : M x K, row-major (K contiguous)
+* B   : "col-major K x N", i.e. stored N x K with K contiguous
+* Bq  : int4 weights stored N x (K/2) bytes; byte t of row n holds k = 2t in
+        bits 3:0 and k = 2t+1 in bits 7:4 (two's-complement nibbles)
+* V   : per (K-group, column) scales, [K/g][N], N contiguous
+* U   : per (K-group, row) scales,    [K/g][M], M contiguous
+* C/D : M x N, row-major
+
+The workloads follow the five configurations the GEMM is benchmarked on
+(dense fp16 256^3, dense bf16 4096^3, decode-shaped bf16, W4A16, grouped MoE).
+Seeds are 1000 + the configuration number (1..5).
+"""
+from __future__ import annotations
+
+import dataclasses
+import numpy as np
+
+F32, F16, BF16, S4 = 0, 1, 2, 3
+DTYPE_NAMES = {F32: "f32", F16: "f16", BF16: "bf16", S4: "s4"}
+
+
+def _round_bits(x: np.ndarray, dtype: int) -> np.ndarray:
+    """Round float32 values once (RN-even) to fp16/bf16 storage bits."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    if dtype == F16:
+        return t.to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    if dtype == BF16:
+        return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    if dtype == F32:
+        return np.ascontiguousarray(x, dtype=np.float32)
+    raise ValueError(f"cannot round to dtype {dtype}")
+
+
+def pack_int4(q: np.ndarray) -> np.ndarray:
+    """Pack signed integers in [-8, 7], shape (N, K) with K even, two per byte.
+
+    Byte t of row n holds k = 2t in the low nibble and k = 2t + 1 in the high
+    nibble, two's complement.  This is storage layout only.
+    """
+    q = np.asarray(q, dtype=np.int64)
+    if q.shape[-1] % 2:
+        raise ValueError("K must be even to pack int4")
+    if q.min(initial=0) < -8 or q.max(initial=0) > 7:
+        raise ValueError("int4 values must lie in [-8, 7]")
+    u = (q & 0xF).astype(np.uint8)
+    return np.ascontiguousarray(u[..., 0::2] | (u[..., 1::2] << 4))
+
+
+@dataclasses.dataclass
+class Problem:
+    """One GEMM instance: raw operand bits plus the scalars."""
+
+    M: int
+    N: int
+    K: int
+    a_type: int
+    b_type: int
+    d_type: int
+    A: np.ndarray
+    B: np.ndarray
+    alpha: float = 1.0
+    beta: float = 0.0
+    c_type: int | None = None
+    C: np.ndarray | None = None
+    V: np.ndarray | None = None      # [K/gb][N]
+    v_type: int | None = None
+    gb: int = 0
+    U: np.ndarray | None = None      # [K/ga][M]
+    u_type: int | None = None
+    ga: int = 0
+    name: str = ""
+
+
+def _rng(seed: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def dense(M, N, K, *, seed, a_type=BF16, d_type=BF16, dist="normal", scale=1.0,
+          alpha=1.0, beta=0.0, c_dist_scale=1.0, name="") -> Problem:
+    """Dense problem.  dist 'uniform' draws U[-1,1]; 'normal' draws N(0, scale^2)."""
+    g = _rng(seed)
+    if dist == "uniform":
+        a = g.uniform(-1.0, 1.0, size=(M, K)).astype(np.float32)
+        b = g.uniform(-1.0, 1.0, size=(N, K)).astype(np.float32)
+    elif dist == "normal":
+        a = (g.standard_normal(size=(M, K), dtype=np.float32) * np.float32(scale))
+        b = (g.standard_normal(size=(N, K), dtype=np.float32) * np.float32(scale))
+    else:
+        raise ValueError(dist)
+    p = Problem(M, N, K, a_type, a_type, d_type, _round_bits(a, a_type), _round_bits(b, a_type),
+                alpha=alpha, beta=beta, name=name)
+    if beta != 0.0:
+        c = g.standard_normal(size=(M, N), dtype=np.float32) * np.float32(c_dist_scale)
+        p.c_type = d_type
+        p.C = _round_bits(c, d_type)
+    return p
+
+
+def config1(seed=1001) -> Problem:
+    """fp16 256^3, uniform[-1,1], fp32 D, alpha 1, beta 0."""
+    return dense(256, 256, 256, seed=seed, a_type=F16, d_type=F32, dist="uniform", name="C1 fp16 256^3")
+
+
+def config2(seed=1002, M=4096, N=4096, K=4096) -> Problem:
+    """bf16 4096^3, N(0,1)/sqrt(K), C bf16 N(0,1), alpha 1.5, beta 0.5, bf16 D."""
+    return dense(M, N, K, seed=seed, a_type=BF16, d_type=BF16, dist="normal",
+                 scale=1.0 / np.sqrt(K), alpha=1.5, beta=0.5, name=f"C2 bf16 {M}x{N}x{K}")
+
+
+def config3(M, seed=1003, N=4096, K=14336) -> Problem:
+    """Decode-shaped bf16: M in {1,16,64}, N 4096, K 14336, N(0, 0.02^2), bf16 D."""
+    return dense(M, N, K, seed=seed + M, a_type=BF16, d_type=BF16, dist="normal", scale=0.02,
+                 name=f"C3 decode M={M}")
+
+
+def w4a16(M, N, K, *, seed, group=128, a_type=BF16, d_type=BF16, vlo=0.005, vhi=0.02,
+          name="") -> Problem:
+    """Int4 weights with fp16 per-(group, column) scales; A ~ N(0,1)."""
+    g = _rng(seed)
+    a = g.standard_normal(size=(M, K), dtype=np.float32)
+    q = g.integers(-8, 8, size=(N, K), dtype=np.int64)
+    v = g.uniform(vlo, vhi, size=(K // group, N)).astype(np.float32)
+    return Problem(M, N, K, a_type, S4, d_type, _round_bits(a, a_type), pack_int4(q),
+                   V=_round_bits(v, F16), v_type=F16, gb=group, name=name or f"W4A16 {M}x{N}x{K}")
+
+
+def config4(seed=1004, M=128, N=11008, K=4096) -> Problem:
+    """W4A16: M 128, K 4096, N 11008, group 128, V uniform[0.005, 0.02] fp16."""
+    return w4a16(M, N, K, seed=seed, name="C4 W4A16")
+
+
+def zipf_counts(tokens: int, experts: int, s: float, seed: int) -> np.ndarray:
+    """Top-1 routing counts: i.i.d. draws from a Zipf(s) law truncated to ranks
+    1..experts, ranks mapped to experts through a seeded permutation."""
+    g = _rng(seed)
+    ranks = np.arange(1, experts + 1, dtype=np.float64)
+    p = ranks ** (-s)
+    p /= p.sum()
+    draws = g.choice(experts, size=tokens, p=p)
+    perm = g.permutation(experts)
+    return np.bincount(perm[draws], minlength=experts).astype(np.int64)
+
+
+@dataclasses.dataclass
+class GroupedProblem:
+    counts: np.ndarray           # tokens per expert
+    offsets: np.ndarray          # [E+1] prefix sums (int32)
+    N: int
+    K: int
+    a_type: int
+    d_type: int
+    A: np.ndarray                # [sum m_e, K] rows sorted by expert
+    B: np.ndarray                # [E, N, K]
+    alpha: float = 1.0
+    beta: float = 0.0
+    name: str = ""
+
+
+def grouped(counts, N, K, *, seed, a_type=BF16, d_type=BF16, a_scale=1.0, b_scale=0.02,
+            name="") -> GroupedProblem:
+    counts = np.asarray(counts, dtype=np.int64)
+    E = len(counts)
+    g = _rng(seed)
+    T = int(counts.sum())
+    a = g.standard_normal(size=(T, K), dtype=np.float32) * np.float32(a_scale)
+    b = g.standard_normal(size=(E, N, K), dtype=np.float32) * np.float32(b_scale)
+    off = np.zeros(E + 1, dtype=np.int32)
+    off[1:] = np.cumsum(counts)
+    return GroupedProblem(counts, off, N, K, a_type, d_type, _round_bits(a, a_type),
+                          _round_bits(b, a_type), name=name)
+
+
+def config5(seed=1005, tokens=4096, experts=8, N=14336, K=4096) -> GroupedProblem:
+    """Grouped MoE: 8 experts, 4096 tokens with Zipf(1.2) counts, N 14336, K 4096."""
+    counts = zipf_counts(tokens, experts, 1.2, seed)
+    return grouped(counts, N, K, seed=seed + 1, name="C5 grouped MoE")
+
+
+def batched(batch, M, N, K, *, seed, a_type=BF16, d_type=BF16, name="") -> GroupedProblem:
+    """Uniform batch: every 'expert' gets M rows (offsets are multiples of M)."""
+    return grouped([M] * batch, N, K, seed=seed, a_type=a_type, d_type=d_type, a_scale=1.0,
+                   b_scale=1.0 / np.sqrt(K), name=name or f"batched {batch}x{M}x{N}x{K}")
