@@ -1,0 +1,626 @@
+// The C ABI (include/gemm.h): handle, operand validation, tensor-map
+// construction, dispatch through the cache / heuristic / measurer, kernel
+// launch, cache export/import.  Host code only; every arithmetic step of the
+// GEMM runs in the CUDA kernels.
+#include "gemm.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <map>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "dispatch.h"
+#include "kparams.h"
+
+using namespace qg;
+
+struct gemm_handle {
+    int device = 0;
+    int sm_count = 0;
+    int cc = 0;
+    std::string name;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    uint32_t* status = nullptr;  // device status words
+    std::map<Key, Choice> cache;
+    std::string last_choice = "none";
+    bool log = false;
+    int force_splitk = 0;
+    uint64_t timeout_ns = 2000000000ull;
+};
+
+namespace {
+
+bool is16(int32_t t) { return t == GEMM_F16 || t == GEMM_BF16; }
+bool is_float_out(int32_t t) { return t == GEMM_F32 || t == GEMM_F16 || t == GEMM_BF16; }
+int64_t elem_bytes_x2(int32_t t) { return t == GEMM_F32 ? 8 : (t == GEMM_S4 ? 1 : 4); }  // 2 * bytes
+
+bool device_pointer(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+// Validate one operand layout against the expected shape and order.
+int check_layout(const gemm_layout_t* d, int32_t order, int64_t rows, int64_t cols) {
+    if (!d) return GEMM_ERR_INVALID_ARG;
+    if (d->order != order) return GEMM_ERR_UNSUPPORTED;
+    if (d->rows != rows || d->cols != cols || d->num < 1) return GEMM_ERR_INVALID_ARG;
+    const int64_t inner = order == GEMM_ROW_MAJOR ? cols : rows;
+    if (d->ld < (inner > 0 ? inner : 1)) return GEMM_ERR_INVALID_ARG;
+    if (d->num > 1 && d->batch_stride < 0) return GEMM_ERR_INVALID_ARG;
+    return GEMM_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* gemm_status_string(int s) {
+    switch (s) {
+        case GEMM_OK: return "ok";
+        case GEMM_ERR_INVALID_ARG: return "invalid argument";
+        case GEMM_ERR_UNSUPPORTED: return "unsupported operand combination or device";
+        case GEMM_ERR_WORKSPACE: return "workspace missing or too small";
+        case GEMM_ERR_CUDA: return "CUDA error";
+        case GEMM_ERR_NO_KERNEL: return "no kernel accepts the problem";
+        case GEMM_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded wait";
+        case GEMM_ERR_BAD_CACHE: return "malformed or foreign dispatch cache";
+        default: return "unknown status";
+    }
+}
+
+int gemm_create(gemm_handle_t* out) {
+    if (!out) return GEMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (prop.major != 10 || prop.minor != 3) return GEMM_ERR_UNSUPPORTED;  // kernels are built for sm_103a
+    gemm_handle* h = new (std::nothrow) gemm_handle;
+    if (!h) return GEMM_ERR_CUDA;
+    h->device = dev;
+    h->sm_count = prop.multiProcessorCount;
+    h->cc = prop.major * 10 + prop.minor;
+    h->name = prop.name;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        cudaGetLastError();
+        delete h;
+        return GEMM_ERR_CUDA;
+    }
+    h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    if (device_status_ptr(&h->status) != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return GEMM_ERR_CUDA;
+    }
+    const char* lg = getenv("GEMM_LOG");
+    h->log = lg && lg[0] && lg[0] != '0';
+    const char* fs = getenv("GEMM_FORCE_SPLITK");
+    if (fs) h->force_splitk = atoi(fs);
+    const char* to = getenv("GEMM_WAIT_TIMEOUT_MS");
+    if (to && atoll(to) > 0) h->timeout_ns = (uint64_t)atoll(to) * 1000000ull;
+    *out = h;
+    return GEMM_OK;
+}
+
+int gemm_destroy(gemm_handle_t h) {
+    delete h;
+    return GEMM_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Tensor map over a [batches][rows][K] operand stored with K contiguous.
+int make_map(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t type, int64_t K, int64_t rows, int64_t ld,
+             int32_t batches, int64_t bstride, int32_t box_rows) {
+    CUtensorMapDataType dt = type == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)batches};
+    cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)bstride * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    const cuuint32_t rank = batches > 1 ? 3 : 2;
+    CUresult r = h->encode(m, dt, rank, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// Tensor map over packed int4 rows: [rows][K/2 bytes], box 32 bytes x rows,
+// no swizzle (the dequantising warps rewrite the tile into the swizzled
+// layout the tensor core reads).
+int make_map_s4(gemm_handle* h, CUtensorMap* m, const void* ptr, int64_t K, int64_t rows, int64_t ld_nibbles,
+                int32_t box_rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld_nibbles / 2)};
+    cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = h->encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_workspace_t* ws, cudaStream_t st) {
+    GemmKernelParams kp;
+    memset(&kp, 0, sizeof kp);
+    kp.sched = make_sched(p, c, h->sm_count);
+    const size_t need_p = partials_bytes_needed(kp.sched, c.bn);
+    const size_t need_c = counters_bytes_needed(kp.sched);
+    if (need_p || need_c) {
+        if (!ws || !ws->partials || !ws->barriers || ws->partials_size < need_p || ws->barriers_size < need_c)
+            return GEMM_ERR_WORKSPACE;
+        if (!aligned16(ws->partials) || (reinterpret_cast<uintptr_t>(ws->barriers) & 3u)) return GEMM_ERR_INVALID_ARG;
+        kp.partials = static_cast<float*>(ws->partials);
+        kp.counters = static_cast<int32_t*>(ws->barriers);
+    }
+    EpiParams& e = kp.epi;
+    e.D = p.D;
+    e.C = p.beta != 0.0f ? p.C : nullptr;
+    e.ldd = p.ldd;
+    e.ldc = p.ldc;
+    e.d_bstride = p.family == FAM_GROUPED ? 0 : p.d_bs;
+    e.c_bstride = p.family == FAM_GROUPED ? 0 : p.c_bs;
+    e.M = p.M;
+    e.N = p.N;
+    e.alpha = p.alpha;
+    e.beta = p.beta;
+    e.d_type = p.d_type;
+    e.swap = c.swap;
+    const int64_t eb = p.d_type == GEMM_F32 ? 4 : 2;
+    e.vec_ok = aligned16(p.D) && (p.ldd * eb) % 16 == 0 &&
+               (e.C == nullptr || (aligned16(p.C) && (p.ldc * eb) % 16 == 0)) &&
+               (p.batches == 1 || ((p.d_bs * eb) % 16 == 0 && (e.C == nullptr || (p.c_bs * eb) % 16 == 0)));
+    kp.idesc = make_idesc_f16(p.a_type == GEMM_BF16, 128, c.bn);
+    kp.status = h->status;
+    kp.timeout_ns = h->timeout_ns;
+
+    CUtensorMap tx, ty;
+    int rc;
+    const bool dq = p.family == FAM_DQ;
+    if (p.family == FAM_GROUPED) {
+        rc = make_map(h, &tx, p.A, p.a_type, p.K, p.M, p.lda, 1, 0, 128);
+        if (rc == GEMM_OK) rc = make_map(h, &ty, p.B, p.b_type, p.K, p.N, p.ldb, p.num_experts, p.b_bs, c.bn);
+        kp.x3d = 0;
+        kp.y3d = 1;
+    } else if (c.swap) {
+        rc = make_map(h, &tx, p.B, p.b_type, p.K, p.N, p.ldb, 1, 0, 128);
+        if (rc == GEMM_OK) rc = make_map(h, &ty, p.A, p.a_type, p.K, p.M, p.lda, 1, 0, c.bn);
+        kp.x3d = kp.y3d = 0;
+    } else {
+        rc = make_map(h, &tx, p.A, p.a_type, p.K, p.M, p.lda, p.batches, p.a_bs, 128);
+        if (rc == GEMM_OK) {
+            if (dq && p.b_type == GEMM_S4)
+                rc = make_map_s4(h, &ty, p.B, p.K, p.N, p.ldb, c.bn);
+            else
+                rc = make_map(h, &ty, p.B, p.b_type, p.K, p.N, p.ldb, p.batches, p.b_bs, c.bn);
+        }
+        kp.x3d = kp.y3d = p.batches > 1;
+    }
+    if (rc != GEMM_OK) return rc;
+    if (dq) {
+        DqParams& d = kp.dq;
+        d.out_bf16 = p.a_type == GEMM_BF16;
+        d.y_int4 = p.b_type == GEMM_S4;
+        d.y_scale = p.V;
+        d.y_scale_ld = p.ldv;
+        d.y_scale_type = p.v_type;
+        d.y_group = p.gb;
+        d.x_scale = p.U;
+        d.x_scale_ld = p.ldu;
+        d.x_scale_type = p.u_type;
+        d.x_group = p.ga;
+        d.y_rows = p.N;
+        d.x_rows = p.M;
+        kp.stages = umma_dq_max_stages(c.bn);
+        if (kp.stages < 2) return GEMM_ERR_NO_KERNEL;
+        cudaError_t ce = launch_umma_dq_gemm(c.bn, tx, ty, kp, kp.sched.programs, st);
+        return ce == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    }
+    kp.stages = umma_max_stages(c.bn);
+    if (kp.stages < 2) return GEMM_ERR_NO_KERNEL;
+    cudaError_t ce = launch_umma_gemm(c.bn, tx, ty, kp, kp.sched.programs, st);
+    return ce == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+bool workspace_fits(gemm_handle* h, const Problem& p, const Choice& c, const gemm_workspace_t* ws) {
+    SchedParams s = make_sched(p, c, h->sm_count);
+    const size_t need_p = partials_bytes_needed(s, c.bn), need_c = counters_bytes_needed(s);
+    if (!need_p && !need_c) return true;
+    return ws && ws->partials && ws->barriers && ws->partials_size >= need_p && ws->barriers_size >= need_c;
+}
+
+// Time one candidate on the stream: one warm-up, then the median of 3.
+float measure(gemm_handle* h, const Problem& p, const Choice& c, const gemm_workspace_t* ws, cudaStream_t st) {
+    cudaEvent_t a, b;
+    if (cudaEventCreate(&a) != cudaSuccess) return -1.0f;
+    if (cudaEventCreate(&b) != cudaSuccess) {
+        cudaEventDestroy(a);
+        return -1.0f;
+    }
+    float best[3] = {-1, -1, -1};
+    bool ok = launch_choice(h, p, c, ws, st) == GEMM_OK;
+    for (int i = 0; ok && i < 3; ++i) {
+        cudaEventRecord(a, st);
+        ok = launch_choice(h, p, c, ws, st) == GEMM_OK;
+        cudaEventRecord(b, st);
+        if (ok && cudaEventSynchronize(b) == cudaSuccess) cudaEventElapsedTime(&best[i], a, b);
+        else ok = false;
+    }
+    cudaEventDestroy(a);
+    cudaEventDestroy(b);
+    if (!ok) {
+        cudaGetLastError();
+        return -1.0f;
+    }
+    std::sort(best, best + 3);
+    return best[1] * 1000.0f;
+}
+
+int dispatch_and_run(gemm_handle* h, const gemm_op_t* op, Problem& p, const gemm_workspace_t* ws, cudaStream_t st) {
+    if (p.M == 0 || p.N == 0) {
+        h->last_choice = "empty";
+        return GEMM_OK;
+    }
+    if (p.K == 0) {  // no products: D = beta * C
+        EpiParams e;
+        memset(&e, 0, sizeof e);
+        e.D = p.D;
+        e.C = p.beta != 0.0f ? p.C : nullptr;
+        e.ldd = p.ldd;
+        e.ldc = p.ldc;
+        e.d_bstride = p.d_bs;
+        e.c_bstride = p.c_bs;
+        e.M = p.M;
+        e.N = p.N;
+        e.alpha = p.alpha;
+        e.beta = p.beta;
+        e.d_type = p.d_type;
+        h->last_choice = "scale_c";
+        return launch_scale_c(e, p.batches, st) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    }
+    Choice c;
+    bool have = false;
+    const int forced_split = op->splitk > 1 ? op->splitk : h->force_splitk;
+    const bool forced = forced_split > 1 || op->splitk == 1 || op->streamk != 0;
+    const Key key = make_key(p);
+    if (!forced && op->dispatch != GEMM_DISPATCH_MEASURE) {
+        auto it = h->cache.find(key);
+        if (it != h->cache.end()) {
+            c = it->second;
+            have = workspace_fits(h, p, c, ws);
+        }
+    }
+    if (!have && !forced && op->dispatch == GEMM_DISPATCH_MEASURE) {
+        auto it = h->cache.find(key);
+        if (it != h->cache.end() && workspace_fits(h, p, it->second, ws)) {
+            c = it->second;
+            have = true;
+        } else if (!(p.beta != 0.0f && p.C == p.D)) {  // timing must not destroy an in-place C
+            float best = -1.0f;
+            for (const Choice& cand : candidates(p, h->sm_count)) {
+                if (!workspace_fits(h, p, cand, ws)) continue;
+                float us = measure(h, p, cand, ws, st);
+                if (us > 0 && (best < 0 || us < best)) {
+                    best = us;
+                    c = cand;
+                    c.us = us;
+                    have = true;
+                }
+            }
+            if (have) h->cache[key] = c;
+        }
+    }
+    if (!have) {
+        c = heuristic(p, h->sm_count);
+        if (forced_split > 1) {
+            c.sched = SCHED_SPLITK;
+            c.splits = forced_split;
+        } else if (op->streamk == 1) {
+            c.sched = SCHED_STREAMK;
+        } else if (op->splitk == 1 || op->streamk == -1) {
+            if (c.sched != SCHED_DP && (op->splitk == 1 || c.sched == SCHED_STREAMK)) c.sched = SCHED_DP;
+        }
+        if (p.family == FAM_GROUPED) c.sched = SCHED_DP;
+        if (!workspace_fits(h, p, c, ws)) {
+            if (forced) return GEMM_ERR_WORKSPACE;
+            c.sched = SCHED_DP;  // automatic choices fall back to no split
+        }
+    }
+    h->last_choice = choice_name(p, c);
+    if (h->log)
+        fprintf(stderr, "qgemm: M=%lld N=%lld K=%lld batches=%d -> %s\n", (long long)p.M, (long long)p.N,
+                (long long)p.K, p.batches, h->last_choice.c_str());
+    int rc = launch_choice(h, p, c, ws, st);
+    if (rc == GEMM_ERR_CUDA) cudaGetLastError();
+    return rc;
+}
+
+// Shared validation of gemm_run / gemm_run_grouped.
+int build_problem(gemm_handle* h, const gemm_op_t* op, float alpha, const void* A, const gemm_layout_t* Adesc,
+                  const void* U, const gemm_layout_t* Udesc, const void* B, const gemm_layout_t* Bdesc,
+                  const void* V, const gemm_layout_t* Vdesc, float beta, const void* C, const gemm_layout_t* Cdesc,
+                  void* D, const gemm_layout_t* Ddesc, bool grouped, Problem* out) {
+    if (!h || !op || !Adesc || !Bdesc || !Ddesc) return GEMM_ERR_INVALID_ARG;
+    if (op->epilogue != 0) return GEMM_ERR_UNSUPPORTED;
+    if (op->dispatch < GEMM_DISPATCH_DEFAULT || op->dispatch > GEMM_DISPATCH_REUSE) return GEMM_ERR_INVALID_ARG;
+    if (op->splitk < 0 || op->streamk < -1 || op->streamk > 1) return GEMM_ERR_INVALID_ARG;
+    if (op->splitk > 1 && op->streamk == 1) return GEMM_ERR_INVALID_ARG;
+    Problem p;
+    memset(&p, 0, sizeof p);
+    p.M = Adesc->rows;
+    p.K = Adesc->cols;
+    p.N = Bdesc->cols;
+    if (p.M < 0 || p.N < 0 || p.K < 0) return GEMM_ERR_INVALID_ARG;
+    if (p.M > INT32_MAX || p.N > INT32_MAX || p.K > INT32_MAX) return GEMM_ERR_INVALID_ARG;
+    p.a_type = Adesc->type;
+    p.b_type = Bdesc->type;
+    p.d_type = Ddesc->type;
+    if (!is16(p.a_type)) return GEMM_ERR_UNSUPPORTED;
+    if (!(p.b_type == p.a_type || p.b_type == GEMM_S4)) return GEMM_ERR_UNSUPPORTED;
+    if (!is_float_out(p.d_type)) return GEMM_ERR_UNSUPPORTED;
+    int rc;
+    if ((rc = check_layout(Adesc, GEMM_ROW_MAJOR, p.M, p.K))) return rc;
+    if ((rc = check_layout(Bdesc, GEMM_COL_MAJOR, p.K, p.N))) return rc;
+    if ((rc = check_layout(Ddesc, GEMM_ROW_MAJOR, p.M, p.N))) return rc;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.A = A;
+    p.lda = Adesc->ld;
+    p.a_bs = Adesc->batch_stride;
+    p.B = B;
+    p.ldb = Bdesc->ld;
+    p.b_bs = Bdesc->batch_stride;
+    p.D = D;
+    p.ldd = Ddesc->ld;
+    p.d_bs = Ddesc->batch_stride;
+    p.batches = Adesc->num;
+    if (beta != 0.0f) {
+        if (!C || !Cdesc) return GEMM_ERR_INVALID_ARG;
+        if ((rc = check_layout(Cdesc, GEMM_ROW_MAJOR, p.M, p.N))) return rc;
+        if (Cdesc->type != p.d_type) return GEMM_ERR_UNSUPPORTED;
+        if (!grouped && Cdesc->num != p.batches) return GEMM_ERR_INVALID_ARG;
+        p.C = C;
+        p.ldc = Cdesc->ld;
+        p.c_bs = Cdesc->batch_stride;
+    }
+    // scale operands: NULL means unscaled
+    if (U) {
+        if (!Udesc || op->quant_a_group <= 0) return GEMM_ERR_INVALID_ARG;
+        p.ga = op->quant_a_group;
+        if (p.ga % 8 || p.K % p.ga) return GEMM_ERR_INVALID_ARG;
+        if (!(is16(Udesc->type) || Udesc->type == GEMM_F32)) return GEMM_ERR_UNSUPPORTED;
+        if ((rc = check_layout(Udesc, GEMM_ROW_MAJOR, p.K / p.ga, p.M))) return rc;
+        if (Udesc->num != 1) return GEMM_ERR_UNSUPPORTED;
+        p.U = U;
+        p.ldu = Udesc->ld;
+        p.u_type = Udesc->type;
+    }
+    if (V) {
+        if (!Vdesc || op->quant_b_group <= 0) return GEMM_ERR_INVALID_ARG;
+        p.gb = op->quant_b_group;
+        if (p.gb % 8 || p.K % p.gb) return GEMM_ERR_INVALID_ARG;
+        if (!(is16(Vdesc->type) || Vdesc->type == GEMM_F32)) return GEMM_ERR_UNSUPPORTED;
+        if ((rc = check_layout(Vdesc, GEMM_ROW_MAJOR, p.K / p.gb, p.N))) return rc;
+        if (Vdesc->num != 1) return GEMM_ERR_UNSUPPORTED;
+        p.V = V;
+        p.ldv = Vdesc->ld;
+        p.v_type = Vdesc->type;
+    }
+    p.family = (p.U || p.V || p.b_type == GEMM_S4) ? FAM_DQ : FAM_DENSE;
+    if (grouped) {
+        if (p.U || p.V || p.b_type == GEMM_S4) return GEMM_ERR_UNSUPPORTED;
+        if (Adesc->num != 1 || Ddesc->num != 1) return GEMM_ERR_INVALID_ARG;
+        p.family = FAM_GROUPED;
+        p.batches = 1;
+    } else {
+        if (Bdesc->num != p.batches || Ddesc->num != p.batches) return GEMM_ERR_INVALID_ARG;
+        if (p.batches > 1 && (p.U || p.V || p.b_type == GEMM_S4)) return GEMM_ERR_UNSUPPORTED;
+        if (p.batches > 1) {
+            if (p.a_bs < p.M * p.lda || p.b_bs < p.N * p.ldb || p.d_bs < p.M * p.ldd) return GEMM_ERR_INVALID_ARG;
+            if (p.C && p.c_bs < 0) return GEMM_ERR_INVALID_ARG;
+        }
+    }
+    if (p.M == 0 || p.N == 0) {
+        *out = p;
+        return GEMM_OK;
+    }
+    if (!D || (p.K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
+    if (p.K > 0) {
+        // operands read by the tensor-memory accelerator
+        if (!aligned16(A) || !aligned16(B)) return GEMM_ERR_INVALID_ARG;
+        if ((p.lda * 2) % 16 || (p.a_bs * 2) % 16) return GEMM_ERR_INVALID_ARG;
+        if (p.b_type == GEMM_S4) {
+            if (p.K % 2 || p.ldb % 32) return GEMM_ERR_INVALID_ARG;
+        } else if ((p.ldb * 2) % 16 || (p.b_bs * 2) % 16) {
+            return GEMM_ERR_INVALID_ARG;
+        }
+        if (!device_pointer(A) || !device_pointer(B)) return GEMM_ERR_INVALID_ARG;
+    }
+    if (!device_pointer(D)) return GEMM_ERR_INVALID_ARG;
+    if (p.C && !device_pointer(p.C)) return GEMM_ERR_INVALID_ARG;
+    (void)elem_bytes_x2;
+    *out = p;
+    return GEMM_OK;
+}
+
+int bind_device(gemm_handle* h) {
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (cur != h->device && cudaSetDevice(h->device) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_run(gemm_handle_t h, const gemm_op_t* op, float alpha, const void* A, const gemm_layout_t* Adesc,
+             const void* U, const gemm_layout_t* Udesc, const void* B, const gemm_layout_t* Bdesc, const void* V,
+             const gemm_layout_t* Vdesc, float beta, const void* C, const gemm_layout_t* Cdesc, void* D,
+             const gemm_layout_t* Ddesc, const gemm_workspace_t* workspace, gemm_stream_t stream) {
+    if (!h) return GEMM_ERR_INVALID_ARG;
+    int rc = bind_device(h);
+    if (rc) return rc;
+    Problem p;
+    rc = build_problem(h, op, alpha, A, Adesc, U, Udesc, B, Bdesc, V, Vdesc, beta, C, Cdesc, D, Ddesc, false, &p);
+    if (rc) return rc;
+    return dispatch_and_run(h, op, p, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gemm_run_grouped(gemm_handle_t h, const gemm_op_t* op, float alpha, const void* A, const gemm_layout_t* Adesc,
+                     const void* U, const gemm_layout_t* Udesc, const void* B, const gemm_layout_t* Bdesc,
+                     const void* V, const gemm_layout_t* Vdesc, float beta, const void* C,
+                     const gemm_layout_t* Cdesc, void* D, const gemm_layout_t* Ddesc,
+                     const int32_t* expert_offsets_dev, int32_t num_experts, const gemm_workspace_t* workspace,
+                     gemm_stream_t stream) {
+    if (!h) return GEMM_ERR_INVALID_ARG;
+    int rc = bind_device(h);
+    if (rc) return rc;
+    if (num_experts < 1 || num_experts > 4096 || !expert_offsets_dev || !Bdesc || Bdesc->num != num_experts)
+        return GEMM_ERR_INVALID_ARG;
+    if (num_experts > 1 && Bdesc->batch_stride < Bdesc->cols * Bdesc->ld) return GEMM_ERR_INVALID_ARG;
+    Problem p;
+    rc = build_problem(h, op, alpha, A, Adesc, U, Udesc, B, Bdesc, V, Vdesc, beta, C, Cdesc, D, Ddesc, true, &p);
+    if (rc) return rc;
+    if (!device_pointer(expert_offsets_dev) || (reinterpret_cast<uintptr_t>(expert_offsets_dev) & 3u))
+        return GEMM_ERR_INVALID_ARG;
+    p.offsets = expert_offsets_dev;
+    p.num_experts = num_experts;
+    return dispatch_and_run(h, op, p, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gemm_export(gemm_handle_t h, void* buf, size_t cap, size_t* written) {
+    if (!h || !written) return GEMM_ERR_INVALID_ARG;
+    const std::string s = cache_serialize(h->cache, h->name, h->sm_count, h->cc);
+    *written = s.size();
+    if (!buf) return GEMM_OK;
+    if (cap < s.size()) return GEMM_ERR_INVALID_ARG;
+    memcpy(buf, s.data(), s.size());
+    return GEMM_OK;
+}
+
+int gemm_import(gemm_handle_t h, const void* buf, size_t size) {
+    if (!h || (!buf && size)) return GEMM_ERR_INVALID_ARG;
+    std::string s(static_cast<const char*>(buf), size);
+    std::map<Key, Choice> merged = h->cache;
+    if (!cache_parse(s, h->name, h->sm_count, h->cc, &merged)) return GEMM_ERR_BAD_CACHE;
+    h->cache.swap(merged);
+    return GEMM_OK;
+}
+
+int gemm_get_tuning_seq(gemm_handle_t h, int32_t* out, int32_t cap, int32_t* n) {
+    if (!h || !n || cap < 0) return GEMM_ERR_INVALID_ARG;
+    const auto& seq = tuning_seq();
+    *n = (int32_t)seq.size();
+    if (out)
+        for (int32_t i = 0; i < cap && i < (int32_t)seq.size(); ++i) out[i] = seq[i];
+    return GEMM_OK;
+}
+
+int gemm_cache_size(gemm_handle_t h, int32_t* n) {
+    if (!h || !n) return GEMM_ERR_INVALID_ARG;
+    *n = (int32_t)h->cache.size();
+    return GEMM_OK;
+}
+
+int gemm_device_status(gemm_handle_t h, gemm_stream_t stream) {
+    if (!h) return GEMM_ERR_INVALID_ARG;
+    int rc = bind_device(h);
+    if (rc) return rc;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    uint32_t st[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(st, h->status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (st[0] == 0) return GEMM_OK;
+    if (h->log)
+        fprintf(stderr, "qgemm: device wait gave up (site %u, block %u, count %u)\n", st[1], st[2], st[3]);
+    if (cudaMemset(h->status, 0, sizeof st) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_ERR_DEVICE_TIMEOUT;
+}
+
+int gemm_selftest_wait_timeout(gemm_handle_t h, uint64_t timeout_ns, gemm_stream_t stream) {
+    if (!h || timeout_ns == 0 || timeout_ns > 10000000000ull) return GEMM_ERR_INVALID_ARG;
+    int rc = bind_device(h);
+    if (rc) return rc;
+    if (launch_wait_selftest(h->status, timeout_ns, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return gemm_device_status(h, stream);
+}
+
+const char* gemm_last_choice(gemm_handle_t h) { return h ? h->last_choice.c_str() : "none"; }
+
+int gemm_plan_streamk(int64_t m, int64_t n, int64_t k, int32_t block_m, int32_t block_n, int32_t block_k,
+                      int32_t total_sm, int64_t out[7]) {
+    if (!out || m < 0 || n < 0 || k < 0 || block_m <= 0 || block_n <= 0 || block_k <= 0 || total_sm <= 0)
+        return GEMM_ERR_INVALID_ARG;
+    StreamKPlan p = streamk_plan(m, n, k, block_m, block_n, block_k, total_sm);
+    out[0] = p.iters_per_tile;
+    out[1] = p.total_tiles;
+    out[2] = p.streamk_tiles;
+    out[3] = p.blocking_tiles;
+    out[4] = p.full_tiles;
+    out[5] = p.partial_tiles;
+    out[6] = p.sm_partition_factor;
+    return GEMM_OK;
+}
+
+int gemm_grouped_block(const int32_t* sizes, int32_t num_experts, int32_t block_m, int64_t block,
+                       int64_t out[3]) {
+    if (!sizes || !out || num_experts < 1 || block_m <= 0 || block < 0) return GEMM_ERR_INVALID_ARG;
+    std::vector<int32_t> off(num_experts + 1, 0);
+    for (int32_t e = 0; e < num_experts; ++e) {
+        if (sizes[e] < 0) return GEMM_ERR_INVALID_ARG;
+        off[e + 1] = off[e] + sizes[e];
+    }
+    int32_t ex, rows;
+    int64_t m0;
+    grouped_block(off.data(), num_experts, block_m, block, &ex, &m0, &rows);
+    out[0] = ex;
+    out[1] = m0;
+    out[2] = rows;
+    return GEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,262 @@
+// Problem analysis, kernel candidates, heuristic and the dispatch-cache text
+// format.  Host only.
+#include "dispatch.h"
+
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <sstream>
+
+#include "kparams.h"
+
+namespace qg {
+
+const std::vector<int32_t>& tuning_seq() {
+    // Batch sizes (M) the dispatch cache is keyed on: dense at small M, where
+    // the best kernel changes quickly, then geometric.
+    static const std::vector<int32_t> seq = {1,   2,   4,    8,    16,   24,   32,   48,   64,   96,
+                                             128, 192, 256,  384,  512,  768,  1024, 1536, 2048, 3072,
+                                             4096, 6144, 8192};
+    return seq;
+}
+
+int64_t m_bucket(int64_t M) {
+    for (int32_t v : tuning_seq())
+        if (M <= v) return v;
+    return ceil_div(M, 8192) * 8192;
+}
+
+Key make_key(const Problem& p) {
+    Key k;
+    k.family = p.family;
+    k.a_type = p.a_type;
+    k.b_type = p.b_type;
+    k.d_type = p.d_type;
+    k.has_c = p.beta != 0.0f;
+    k.has_u = p.U != nullptr;
+    k.has_v = p.V != nullptr;
+    k.ga = p.U ? p.ga : 0;
+    k.gb = p.V ? p.gb : 0;
+    k.m_bucket = m_bucket(p.M);
+    k.N = p.N;
+    k.K = p.K;
+    k.batches = p.batches;
+    return k;
+}
+
+SchedParams make_sched(const Problem& p, const Choice& c, int sm_count) {
+    SchedParams s;
+    memset(&s, 0, sizeof s);
+    s.k_iters = (int32_t)ceil_div(p.K, BK_HOST);
+    s.batches = p.batches;
+    if (p.family == FAM_GROUPED) {
+        // upper bound on padded M-blocks: sum_e ceil(m_e / 128) <= T / 128 + E
+        s.tiles_x = (int32_t)(p.M / 128 + p.num_experts);
+        s.tiles_y = (int32_t)ceil_div(p.N, c.bn);
+        s.batches = 1;
+        s.grouped = 1;
+        s.expert_offsets = p.offsets;
+        s.num_experts = p.num_experts;
+    } else if (c.swap) {
+        s.tiles_x = (int32_t)ceil_div(p.N, 128);
+        s.tiles_y = (int32_t)ceil_div(p.M, c.bn);
+    } else {
+        s.tiles_x = (int32_t)ceil_div(p.M, 128);
+        s.tiles_y = (int32_t)ceil_div(p.N, c.bn);
+    }
+    const int64_t T = total_tiles(s);
+    s.splits = 1;
+    s.chunk = s.k_iters;
+    s.kind = c.sched;
+    if (c.sched == SCHED_SPLITK) {
+        int32_t S = c.splits < 1 ? 1 : c.splits;
+        if (S > s.k_iters) S = s.k_iters;
+        int32_t chunk = (int32_t)ceil_div(s.k_iters, S);
+        S = (int32_t)ceil_div(s.k_iters, chunk);
+        s.splits = S;
+        s.chunk = chunk;
+        int64_t units = T * S;
+        s.programs = (int32_t)(units < sm_count ? units : sm_count);
+        if (S == 1) s.kind = SCHED_DP;
+    } else if (c.sched == SCHED_STREAMK) {
+        int64_t iters = T * s.k_iters;
+        s.programs = (int32_t)(iters < sm_count ? iters : sm_count);
+        StreamKPlan pl = streamk_plan((int64_t)s.tiles_x * 128, (int64_t)s.tiles_y * c.bn * s.batches, p.K, 128,
+                                      c.bn, BK_HOST, s.programs);
+        s.sk_tiles = (int32_t)pl.streamk_tiles;
+        s.sk_full = (int32_t)pl.full_tiles;
+        s.sk_partial = (int32_t)pl.partial_tiles;
+        s.sk_factor = (int32_t)pl.sm_partition_factor;
+    } else {
+        s.kind = SCHED_DP;
+        s.programs = (int32_t)(T < sm_count ? T : sm_count);
+    }
+    if (s.programs < 1) s.programs = 1;
+    return s;
+}
+
+size_t partials_bytes_needed(const SchedParams& s, int bn) {
+    return (size_t)partial_slots_needed(s) * 128 * (size_t)bn * sizeof(float);
+}
+
+size_t counters_bytes_needed(const SchedParams& s) {
+    if (s.kind == SCHED_DP) return 0;
+    return (size_t)total_tiles(s) * sizeof(int32_t);
+}
+
+static int32_t swap_bn(int64_t M) {
+    if (M <= 16) return 16;
+    if (M <= 32) return 32;
+    if (M <= 64) return 64;
+    return 128;
+}
+
+static bool swap_allowed(const Problem& p) {
+    return p.family == FAM_DENSE && p.batches == 1 && p.M <= 128;
+}
+
+std::vector<Choice> candidates(const Problem& p, int sm_count) {
+    std::vector<Choice> out;
+    const int64_t k_iters = ceil_div(p.K, BK_HOST);
+    auto add_scheds = [&](int32_t bn, int32_t swap) {
+        Choice c;
+        c.bn = bn;
+        c.swap = swap;
+        c.sched = SCHED_DP;
+        out.push_back(c);
+        if (p.family == FAM_GROUPED) return;
+        SchedParams s = make_sched(p, c, sm_count);
+        const int64_t T = total_tiles(s);
+        if (k_iters >= 2 && T < 4 * (int64_t)sm_count) {
+            c.sched = SCHED_STREAMK;
+            out.push_back(c);
+        }
+        if (T < sm_count) {
+            for (int32_t S : {2, 4, 8}) {
+                if (k_iters < 2 * S) break;
+                c.sched = SCHED_SPLITK;
+                c.splits = S;
+                out.push_back(c);
+            }
+        }
+    };
+    if (p.family == FAM_DQ) {
+        for (int32_t bn : {64, 128, 256})
+            if (bn == 64 || p.N > bn / 2) add_scheds(bn, 0);
+        return out;
+    }
+    add_scheds(128, 0);
+    if (p.N > 128) add_scheds(256, 0);
+    if (swap_allowed(p)) add_scheds(swap_bn(p.M), 1);
+    return out;
+}
+
+Choice heuristic(const Problem& p, int sm_count) {
+    Choice c;
+    if (swap_allowed(p) && p.M <= 64) {
+        c.swap = 1;
+        c.bn = swap_bn(p.M);
+    } else {
+        c.bn = p.N > 128 ? 256 : 128;
+        if (p.family == FAM_DQ) c.bn = 128;
+    }
+    c.sched = SCHED_DP;
+    if (p.family == FAM_GROUPED) return c;
+    SchedParams s = make_sched(p, c, sm_count);
+    const int64_t T = total_tiles(s);
+    const int64_t k_iters = s.k_iters;
+    const double waves = (double)T / sm_count;
+    const double eff = waves / ceil(waves);
+    if (k_iters >= 4 && eff < 0.9) c.sched = SCHED_STREAMK;
+    return c;
+}
+
+std::string choice_name(const Problem& p, const Choice& c) {
+    char buf[96];
+    const char* fam = p.family == FAM_DQ ? "umma_dq" : (p.family == FAM_GROUPED ? "umma_grouped" : "umma");
+    const char* sk = c.sched == SCHED_DP ? "dp" : (c.sched == SCHED_STREAMK ? "streamk" : "splitk");
+    if (c.sched == SCHED_SPLITK)
+        snprintf(buf, sizeof buf, "%s_bn%d%s/%s%d", fam, c.bn, c.swap ? "_swap" : "", sk, c.splits);
+    else
+        snprintf(buf, sizeof buf, "%s_bn%d%s/%s", fam, c.bn, c.swap ? "_swap" : "", sk);
+    return buf;
+}
+
+// ---- cache text format ------------------------------------------------------------
+//
+//   qgemm-dispatch-cache 1
+//   device <name, spaces as '_'> sm <count> cc <major*10+minor>
+//   entries <n>
+//   <family> <a> <b> <d> <has_c> <has_u> <has_v> <ga> <gb> <m_bucket> <N> <K> <batches> : <bn> <swap> <sched> <splits> <us>
+//   ...
+//   end
+
+static std::string sanitize(const std::string& s) {
+    std::string r = s;
+    for (char& ch : r)
+        if (ch == ' ' || ch == '\t' || ch == '\n') ch = '_';
+    return r.empty() ? "unknown" : r;
+}
+
+std::string cache_serialize(const std::map<Key, Choice>& cache, const std::string& device, int sm, int cc) {
+    std::ostringstream os;
+    os << "qgemm-dispatch-cache 1\n";
+    os << "device " << sanitize(device) << " sm " << sm << " cc " << cc << "\n";
+    os << "entries " << cache.size() << "\n";
+    for (const auto& kv : cache) {
+        const Key& k = kv.first;
+        const Choice& c = kv.second;
+        char us[32];
+        snprintf(us, sizeof us, "%.3f", c.us);
+        os << k.family << ' ' << k.a_type << ' ' << k.b_type << ' ' << k.d_type << ' ' << k.has_c << ' ' << k.has_u
+           << ' ' << k.has_v << ' ' << k.ga << ' ' << k.gb << ' ' << k.m_bucket << ' ' << k.N << ' ' << k.K << ' '
+           << k.batches << " : " << c.bn << ' ' << c.swap << ' ' << c.sched << ' ' << c.splits << ' ' << us
+           << "\n";
+    }
+    os << "end\n";
+    return os.str();
+}
+
+static bool valid_choice(const Key& k, const Choice& c) {
+    const bool bn_ok = c.bn == 16 || c.bn == 32 || c.bn == 64 || c.bn == 128 || c.bn == 256;
+    if (!bn_ok || (c.swap != 0 && c.swap != 1) || c.sched < SCHED_DP || c.sched > SCHED_STREAMK) return false;
+    if (c.splits < 1 || c.splits > 64 || !(c.us >= 0.0f)) return false;
+    if (k.family < FAM_DENSE || k.family > FAM_GROUPED) return false;
+    if (k.N < 0 || k.K < 0 || k.m_bucket < 1 || k.batches < 1) return false;
+    return true;
+}
+
+bool cache_parse(const std::string& text, const std::string& device, int sm, int cc, std::map<Key, Choice>* out) {
+    std::istringstream is(text);
+    std::string magic, word, dev;
+    int version = 0, sm_in = -1, cc_in = -1;
+    long long n = -1;
+    if (!(is >> magic >> version) || magic != "qgemm-dispatch-cache" || version != 1) return false;
+    if (!(is >> word) || word != "device" || !(is >> dev)) return false;
+    if (!(is >> word) || word != "sm" || !(is >> sm_in)) return false;
+    if (!(is >> word) || word != "cc" || !(is >> cc_in)) return false;
+    if (dev != sanitize(device) || sm_in != sm || cc_in != cc) return false;
+    if (!(is >> word) || word != "entries" || !(is >> n) || n < 0 || n > 1000000) return false;
+    std::map<Key, Choice> tmp;
+    for (long long i = 0; i < n; ++i) {
+        Key k;
+        Choice c;
+        std::string colon;
+        long long mb, N, K;
+        if (!(is >> k.family >> k.a_type >> k.b_type >> k.d_type >> k.has_c >> k.has_u >> k.has_v >> k.ga >> k.gb >>
+              mb >> N >> K >> k.batches >> colon >> c.bn >> c.swap >> c.sched >> c.splits >> c.us))
+            return false;
+        if (colon != ":") return false;
+        k.m_bucket = mb;
+        k.N = N;
+        k.K = K;
+        if (!valid_choice(k, c)) return false;
+        tmp[k] = c;
+    }
+    if (!(is >> word) || word != "end") return false;
+    for (const auto& kv : tmp) (*out)[kv.first] = kv.second;
+    return true;
+}
+
+}  // namespace qg

@@ -1,0 +1,91 @@
+// Parameter blocks handed from the host dispatcher to the kernels.  Plain
+// structs of integers and pointers, passed by value as kernel parameters.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "work_sched.h"
+
+namespace qg {
+
+enum DType : int32_t { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2, DT_S4 = 3 };
+
+// Where a bounded wait gave up (recorded in the device status word).
+enum WaitSite : uint32_t {
+    SITE_PRODUCER_EMPTY = 1,
+    SITE_MMA_FULL = 2,
+    SITE_MMA_TMEM_EMPTY = 3,
+    SITE_EPI_TMEM_FULL = 4,
+    SITE_DRAIN = 5,
+    SITE_DQ_RAW = 6,
+    SITE_DQ_EMPTY = 7,
+    SITE_MMA_OPERAND = 8,
+    SITE_SELFTEST = 9,
+};
+
+// Epilogue: D = fma(alpha, acc, beta * C) rounded to D's type.
+struct EpiParams {
+    void* D;
+    const void* C;     // NULL when beta == 0 (never read then)
+    int64_t ldd, ldc;  // elements
+    int64_t d_bstride, c_bstride;  // elements between batches (0 for grouped)
+    int64_t M, N;      // output rows / columns (per batch)
+    float alpha, beta;
+    int32_t d_type;    // DT_F32 / DT_F16 / DT_BF16 (C has the same type)
+    int32_t swap;      // 0: tile rows are D rows; 1: tile rows are D columns
+    int32_t vec_ok;    // C/D bases and ld allow 16-byte vector access
+};
+
+// Group-wise scale / dequantisation applied to the shared-memory operands
+// before the tensor core reads them (the "GroupIter" role of the pages).
+struct DqParams {
+    // Y operand (UMMA N side, "B" of a non-swapped GEMM)
+    const void* y_scale;     // [K/gy][y_rows] scales, y_rows contiguous, or NULL
+    int64_t y_scale_ld;      // elements
+    int32_t y_scale_type;    // DT_F16 / DT_BF16 / DT_F32
+    int32_t y_group;         // group size along K
+    int32_t y_int4;          // Y is packed int4 (raw tile is BN x 32 bytes)
+    // X operand (UMMA M side, "A" of a non-swapped GEMM)
+    const void* x_scale;     // [K/gx][x_rows] or NULL
+    int64_t x_scale_ld;
+    int32_t x_scale_type;
+    int32_t x_group;
+    int32_t out_bf16;        // the rounded operand type: 1 bf16, 0 f16
+    int64_t y_rows, x_rows;  // rows of the scaled operands (for bounds)
+};
+
+struct GemmKernelParams {
+    SchedParams sched;
+    EpiParams epi;
+    DqParams dq;
+    uint32_t idesc;       // tcgen05.mma instruction descriptor
+    int32_t x3d, y3d;     // the X / Y tensor maps take a batch coordinate
+    int32_t stages;       // shared-memory ring depth
+    float* partials;      // fp32 partial tiles (split-K / stream-K)
+    int32_t* counters;    // per-tile arrival counters (self-resetting)
+    uint32_t* status;     // device status words [4]
+    uint64_t timeout_ns;  // bound on every wait
+};
+
+// Instruction descriptor of tcgen05.mma.kind::f16: fp32 accumulator (bits
+// 4-5 = 1), A/B format (bits 7-9 / 10-12: 0 = f16, 1 = bf16), both operands
+// K-major (bits 15, 16 = 0), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+QG_HD uint32_t make_idesc_f16(int ab_is_bf16, int m, int n) {
+    uint32_t fmt = ab_is_bf16 ? 1u : 0u;
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+// Entry points implemented in the .cu files.
+cudaError_t launch_umma_gemm(int bn, const CUtensorMap& tx, const CUtensorMap& ty, const GemmKernelParams& p,
+                             int grid, cudaStream_t st);
+cudaError_t launch_umma_dq_gemm(int bn, const CUtensorMap& tx, const CUtensorMap& ty, const GemmKernelParams& p,
+                                int grid, cudaStream_t st);
+cudaError_t launch_scale_c(const EpiParams& e, int64_t batches, cudaStream_t st);
+cudaError_t launch_wait_selftest(uint32_t* status, uint64_t timeout_ns, cudaStream_t st);
+int umma_max_stages(int bn);
+int umma_dq_max_stages(int bn);
+cudaError_t device_status_ptr(uint32_t** out);
+
+}  // namespace qg

@@ -1,0 +1,124 @@
+"""Shared helpers for the GPU parity tests: move synth problems to the device,
+call the library through its C ABI, and compare with the oracle under the
+acceptance rule
+
+    |D - ref| <= 1e-5 * S + 1e-6                 (fp32 D)
+    |D - ref| <= 1e-5 * S + 1e-6 + ulp_D(ref)    (fp16 / bf16 D)
+
+where S = |alpha| * sum_k |a_ik * b_kj| + |beta * c_ij| is returned by the
+oracle alongside ref.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+import quantized_gemm_tcgen05_gb300 as qg
+import oracle
+import synth
+
+TORCH_DT = {synth.F32: torch.float32, synth.F16: torch.float16, synth.BF16: torch.bfloat16}
+
+
+def dev_bits(bits, dtype):
+    """numpy storage bits -> device tensor of the storage dtype."""
+    if dtype == synth.F32:
+        return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.float32)).cuda()
+    if dtype == synth.S4:
+        return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint8)).cuda()
+    t = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16))
+    return t.view(TORCH_DT[dtype]).cuda()
+
+
+def tolerance(ref, bound, d_type):
+    tol = 1e-5 * bound + 1e-6
+    if d_type != synth.F32:
+        tol = tol + oracle.ulp(d_type, ref)
+    return tol
+
+
+def assert_close(d, ref, bound, d_type, what=""):
+    d = np.asarray(d, dtype=np.float64)
+    tol = tolerance(ref, bound, d_type)
+    err = np.abs(d - ref)
+    bad = ~(err <= tol)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        msg = ", ".join(f"{tuple(i)}: got {d[tuple(i)]!r} ref {ref[tuple(i)]!r} tol {tol[tuple(i)]:.3g}"
+                        for i in idx)
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; {msg}")
+
+
+class Lib:
+    """A handle plus a workspace on the current device."""
+
+    def __init__(self):
+        self.h = qg.gemm_create()
+        self.ws = qg.Workspace()
+
+    def close(self):
+        qg.gemm_destroy(self.h)
+
+
+def op(dispatch=0, splitk=0, streamk=0, ga=0, gb=0):
+    return qg.gemm_op_t(dispatch, 0, ga, gb, splitk, streamk)
+
+
+def run_problem(lib, p, o=None, D=None, C=None, stream=None, workspace=True):
+    """Run a synth.Problem through gemm_run.  Returns (status, D tensor)."""
+    o = o or op(ga=p.ga if p.U is not None else 0, gb=p.gb if p.V is not None else 0)
+    A = dev_bits(p.A, p.a_type)
+    B = dev_bits(p.B, p.b_type)
+    Ad = qg.row_major(A)
+    Bd = qg.col_major_from_nk(B, k=p.K, type_=p.b_type)
+    if D is None:
+        D = torch.full((p.M, p.N), float("nan"), dtype=TORCH_DT[p.d_type], device="cuda")
+    Dd = qg.row_major(D)
+    Cd = None
+    if p.beta != 0.0 and C is None:
+        C = dev_bits(p.C, p.c_type)
+    if C is not None:
+        Cd = qg.row_major(C)
+    U = Ud = V = Vd = None
+    if p.U is not None:
+        U = dev_bits(p.U, p.u_type)
+        Ud = qg.layout(p.u_type, qg.GEMM_ROW_MAJOR, p.K // p.ga, p.M, p.M)
+    if p.V is not None:
+        V = dev_bits(p.V, p.v_type)
+        Vd = qg.layout(p.v_type, qg.GEMM_ROW_MAJOR, p.K // p.gb, p.N, p.N)
+    st = stream if stream is not None else qg.current_stream()
+    rc = qg.gemm_run(lib.h, o, p.alpha, qg.ptr(A), Ad, qg.ptr(U), Ud, qg.ptr(B), Bd, qg.ptr(V), Vd, p.beta,
+                     qg.ptr(C), Cd, qg.ptr(D), Dd, lib.ws.c if workspace else None, st)
+    torch.cuda.synchronize()
+    return rc, D
+
+
+def grouped_to_device(gp):
+    A = dev_bits(gp.A, gp.a_type)
+    B = dev_bits(gp.B, gp.a_type)
+    off = torch.from_numpy(gp.offsets.astype(np.int32)).cuda()
+    return A, B, off
+
+
+def run_grouped(lib, gp, o=None, A=None, B=None, off=None):
+    if A is None:
+        A, B, off = grouped_to_device(gp)
+    T = int(gp.offsets[-1])
+    D = torch.full((T, gp.N), float("nan"), dtype=TORCH_DT[gp.d_type], device="cuda")
+    rc = qg.gemm_run_grouped(lib.h, o or op(), gp.alpha, qg.ptr(A), qg.row_major(A), None, None, qg.ptr(B),
+                             qg.col_major_from_nk(B), None, None, gp.beta, None, None, qg.ptr(D), qg.row_major(D),
+                             qg.ptr(off), len(gp.counts), lib.ws.c, qg.current_stream())
+    torch.cuda.synchronize()
+    return rc, D
+
+
+def sample_indices(M, N, n, seed):
+    """Sampled (i, j) positions covering corners, tile edges and random interior."""
+    rng = np.random.default_rng(seed)
+    fixed_i = [0, M - 1, min(127, M - 1), min(128, M - 1), M // 2]
+    fixed_j = [0, N - 1, min(255, N - 1), min(256, N - 1), N // 2]
+    ii = np.concatenate([np.repeat(fixed_i, len(fixed_j)), rng.integers(0, M, n)])
+    jj = np.concatenate([np.tile(fixed_j, len(fixed_i)), rng.integers(0, N, n)])
+    return ii, jj
