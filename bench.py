@@ -1,0 +1,504 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 GEMM library.
+
+Default workload (one step = one gemm_run through the C ABI): the dense bf16
+GEMM M = N = K = 4096, A row-major, B col-major, entries N(0,1)/sqrt(K),
+C bf16 N(0,1), alpha 1.5, beta 0.5, bf16 D, fp32 accumulation.  Metric:
+TFLOP/s = 2*M*N*K / time.  Three rotating input sets (384 MB) keep the
+operands out of the 129 MB L2 between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config c2|c1|c3m1|c3m16|c3m64|c4|c5]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the GEMM has no exchange step), timing is the max over ranks and the value
+is the total work of all ranks divided by it.  ``--impl reference`` times the
+CPU oracle (the only reference this project has) on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---- workloads ----------------------------------------------------------------------
+
+WORKLOADS = {
+    "c1": dict(desc="dense fp16 GEMM M=N=K=256, fp32 D, alpha 1 beta 0", kind="dense"),
+    "c2": dict(desc="dense bf16 GEMM M=N=K=4096, A row-major, B col-major, N(0,1)/sqrt(K), C bf16 N(0,1), "
+                    "alpha 1.5 beta 0.5, bf16 D", kind="dense"),
+    "c3m1": dict(desc="decode bf16 GEMM M=1 N=4096 K=14336, N(0,0.02), bf16 D", kind="dense", M=1),
+    "c3m16": dict(desc="decode bf16 GEMM M=16 N=4096 K=14336, N(0,0.02), bf16 D", kind="dense", M=16),
+    "c3m64": dict(desc="decode bf16 GEMM M=64 N=4096 K=14336, N(0,0.02), bf16 D", kind="dense", M=64),
+    "c4": dict(desc="W4A16 GEMM M=128 K=4096 N=11008, int4 B + fp16 group-128 scales, bf16 D", kind="dense"),
+    "c5": dict(desc="grouped MoE bf16 GEMM, 8 experts, 4096 tokens Zipf(1.2), K=4096, N=14336, bf16 D",
+               kind="grouped"),
+}
+
+
+def make_problem(cfg):
+    if cfg == "c1":
+        return synth.config1()
+    if cfg == "c2":
+        return synth.config2()
+    if cfg.startswith("c3m"):
+        return synth.config3(int(cfg[3:]))
+    if cfg == "c4":
+        return synth.config4()
+    if cfg == "c5":
+        return synth.config5()
+    raise ValueError(cfg)
+
+
+def flops_of(p):
+    if hasattr(p, "counts"):
+        return 2.0 * int(p.offsets[-1]) * p.N * p.K
+    return 2.0 * p.M * p.N * p.K
+
+
+def algorithmic_bytes(p):
+    """A, B (packed for int4), U/V, C (if beta != 0) and D, each once."""
+    if hasattr(p, "counts"):
+        T = int(p.offsets[-1])
+        experts = int((p.counts > 0).sum())
+        return 2 * (T * p.K + experts * p.N * p.K + T * p.N)
+    out_b = 4 if p.d_type == synth.F32 else 2
+    b = 2 * p.M * p.K + out_b * p.M * p.N
+    b += p.N * p.K // 2 if p.b_type == synth.S4 else 2 * p.N * p.K
+    if p.V is not None:
+        b += p.V.size * (4 if p.v_type == synth.F32 else 2)
+    if p.beta != 0.0:
+        b += out_b * p.M * p.N
+    return b
+
+
+def metric_of(cfg):
+    """(metric, unit, bound) per workload: HBM-bound ones report GB/s."""
+    if cfg.startswith("c3"):
+        return "GEMM HBM GB/s (decode)", "GB/s", "hbm"
+    return "GEMM TFLOP/s", "TFLOP/s", "tensor"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_gemm_tcgen05_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(cfg):
+    """Per-launch DRAM bytes from the committed ncu summary of this workload,
+    or None when it is missing or was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"umma_gemm_{cfg}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+# ---- clocks -------------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples, kept for a time window."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [r for t, r in self.rows if t0 <= t <= t1 + 0.1]
+        if not rows:
+            rows = [r for _, r in self.rows[-3:]]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[2]) for r in rows if len(r) > 3 and r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if len(r) > 3 and r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for i, n in enumerate(names):
+                if len(r) > 6 + i and r[6 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---- our implementation ---------------------------------------------------------------
+
+class Runner:
+    """Device buffers plus pre-built ctypes arguments for repeated gemm_run calls."""
+
+    def __init__(self, p, sets, qg, torch):
+        self.p, self.qg, self.torch = p, qg, torch
+        self.h = qg.gemm_create()
+        self.ws = qg.Workspace()
+        self.op = qg.gemm_op_t(0, 0, 0, p.gb if getattr(p, "V", None) is not None else 0, 0, 0)
+        self.stream = qg.current_stream()
+        self.grouped = hasattr(p, "counts")
+        self.args = []
+        self.bufs = []
+        for s in range(sets):
+            self.args.append(self._build(s))
+
+    def _dev(self, bits, dtype):
+        torch = self.torch
+        if dtype == synth.S4:
+            return torch.from_numpy(np.ascontiguousarray(bits)).cuda()
+        if dtype == synth.F32:
+            return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.float32)).cuda()
+        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+        return t.view(torch.bfloat16 if dtype == synth.BF16 else torch.float16).cuda()
+
+    def _build(self, s):
+        qg, torch, p = self.qg, self.torch, self.p
+        if self.grouped:
+            A, B = self._dev(p.A, p.a_type), self._dev(p.B, p.a_type)
+            off = torch.from_numpy(p.offsets.astype(np.int32)).cuda()
+            T = int(p.offsets[-1])
+            D = torch.empty(T, p.N, dtype=torch.bfloat16, device="cuda")
+            self.bufs.append((A, B, off, D))
+            return dict(A=A, B=B, off=off, D=D, Ad=qg.row_major(A), Bd=qg.col_major_from_nk(B), Dd=qg.row_major(D))
+        A = self._dev(p.A, p.a_type)
+        B = self._dev(p.B, p.b_type)
+        dt = {synth.F32: torch.float32, synth.F16: torch.float16, synth.BF16: torch.bfloat16}[p.d_type]
+        D = torch.empty(p.M, p.N, dtype=dt, device="cuda")
+        C = self._dev(p.C, p.c_type) if p.beta != 0.0 else None
+        V = self._dev(p.V, p.v_type) if p.V is not None else None
+        self.bufs.append((A, B, C, D, V))
+        d = dict(A=A, B=B, C=C, D=D, V=V, Ad=qg.row_major(A), Bd=qg.col_major_from_nk(B, k=p.K, type_=p.b_type),
+                 Dd=qg.row_major(D), Cd=qg.row_major(C) if C is not None else None,
+                 Vd=qg.layout(p.v_type, qg.GEMM_ROW_MAJOR, p.K // p.gb, p.N, p.N) if V is not None else None)
+        return d
+
+    def run(self, s):
+        qg, p, a = self.qg, self.p, self.args[s]
+        if self.grouped:
+            rc = qg.gemm_run_grouped(self.h, self.op, p.alpha, a["A"].data_ptr(), a["Ad"], None, None,
+                                     a["B"].data_ptr(), a["Bd"], None, None, p.beta, None, None, a["D"].data_ptr(),
+                                     a["Dd"], a["off"].data_ptr(), len(p.counts), self.ws.c, self.stream)
+        else:
+            rc = qg.gemm_run(self.h, self.op, p.alpha, a["A"].data_ptr(), a["Ad"], None, None, a["B"].data_ptr(),
+                             a["Bd"], qg.ptr(a["V"]), a["Vd"], p.beta, qg.ptr(a["C"]), a["Cd"], a["D"].data_ptr(),
+                             a["Dd"], self.ws.c, self.stream)
+        if rc:
+            raise RuntimeError(f"gemm_run failed: {qg.gemm_status_string(rc)}")
+
+
+def run_ours(args, rank, world, cfg):
+    import torch
+
+    import quantized_gemm_tcgen05_gb300 as qg
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    p = make_problem(cfg)
+    flops = flops_of(p)
+    abytes = algorithmic_bytes(p)
+    metric, unit, bound = metric_of(cfg)
+    unit_per_step = abytes / 1e9 if unit == "GB/s" else flops / 1e12
+    one_set = abytes
+    sets = max(1, min(8, int(np.ceil(3 * 129e6 / max(one_set, 1)))))
+    sets = 3 if cfg == "c2" else sets
+    R = Runner(p, sets, qg, torch)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(1.5)  # nvidia-smi needs a moment before its first sample
+    for i in range(args.warmup):
+        R.run(i % sets)
+    torch.cuda.synchronize()
+    if qg.gemm_device_status(R.h, R.stream):
+        raise RuntimeError("device status reported a timeout during warm-up")
+    choice = qg.gemm_last_choice(R.h)
+
+    # timed region: K steps, events around every launch on the launching stream
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        R.run(i % sets)
+        evs[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t1 = time.time()
+    sampler.stop()
+    total_ms = start.elapsed_time(end)
+    launch_ms = [a.elapsed_time(b) for a, b in evs]
+    if dist is not None:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * unit_per_step * args.steps / (total_ms / 1e3)
+    if qg.gemm_device_status(R.h, R.stream):
+        raise RuntimeError("device status reported a timeout during the timed region")
+
+    # end-to-end through the C ABI with host buffers: H2D of this step's
+    # inputs from pinned memory, the GEMM, D2H of the result, every step
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(R, torch, unit_per_step, unit, world, dist, steps=max(3, min(20, args.steps)))
+
+    peaks, peak_src = load_peaks()
+    avg_launch_s = statistics.mean(launch_ms) / 1e3
+    if bound == "hbm":
+        achieved = abytes / avg_launch_s / 1e9
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        r_unit = "GB/s"
+    else:
+        achieved = flops / avg_launch_s / 1e12
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        r_unit = "TFLOP/s"
+    traffic = profile_traffic(cfg)
+    clocks = sampler.summary(t0, t1)
+    line = {
+        "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if p.a_type == synth.BF16 else "f16",
+        "data": "synthetic (seeded, shapes and distributions of the workload)",
+        "config": {"workload": WORKLOADS[cfg]["desc"], "kernel": choice, "parallelism": f"replicas x{world}",
+                   "l2": f"{sets} rotating input sets ({sets * one_set / 1e6:.0f} MB) so operands are not L2-resident"},
+        "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": r_unit,
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})",
+                     "algorithmic_per_launch": abytes if bound == "hbm" else flops,
+                     "avg_launch_us": round(avg_launch_s * 1e6, 3)},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+    }
+    if bound == "tensor":
+        hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        line["roofline"]["hbm_gbs"] = round(abytes / avg_launch_s / 1e9, 1)
+        line["roofline"]["min_roofline_us"] = round(max(flops / (peak * 1e12), abytes / (hbm_peak * 1e9)) * 1e6, 3)
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(p, cfg, unit)
+    if dist is not None:
+        dist.destroy_process_group()
+    R.qg.gemm_destroy(R.h)
+    return line
+
+
+def measure_e2e(R, torch, unit_per_step, unit, world, dist, steps):
+    stream = torch.cuda.current_stream()
+    a = R.args[0]
+    host = {}
+    h2d = 0
+    names = ["A", "B", "C", "V", "off"] if not R.grouped else ["A", "B", "off"]
+    for n in names:
+        t = a.get(n)
+        if t is None:
+            continue
+        host[n] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        host[n].copy_(t)
+        h2d += t.numel() * t.element_size()
+    D = a["D"]
+    hD = torch.empty(D.shape, dtype=D.dtype, pin_memory=True)
+    d2h = D.numel() * D.element_size()
+    torch.cuda.synchronize()
+
+    def step():
+        for n, h in host.items():
+            a[n].copy_(h, non_blocking=True)
+        R.run(0)
+        hD.copy_(D, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    s.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e)
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": round(world * unit_per_step * steps / (ms / 1e3), 3), "unit": unit,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms / steps, 4)}
+
+
+# ---- the CPU oracle as baseline / reference arm ---------------------------------------------
+
+def oracle_sample(p, rows):
+    """The first `rows` rows of the problem (all columns, full K) -- a bounded
+    sample for the CPU oracle."""
+    import copy
+
+    if hasattr(p, "counts"):
+        e = int(np.argmax(p.counts))
+        lo = int(p.offsets[e])
+        q = synth.Problem(min(rows, int(p.counts[e])), p.N, p.K, p.a_type, p.a_type, p.d_type,
+                          p.A[lo:lo + rows], p.B[e], alpha=p.alpha, beta=p.beta)
+        return q
+    q = copy.copy(p)
+    q.M = min(rows, p.M)
+    q.A = p.A[:q.M]
+    if p.C is not None:
+        q.C = p.C[:q.M]
+    return q
+
+
+def cpu_baseline(p, cfg, unit, target_s=12.0):
+    import oracle
+
+    rows = 8
+    q = oracle_sample(p, rows)
+    t = time.perf_counter()
+    oracle.gemm(q)
+    dt = time.perf_counter() - t
+    if dt < target_s / 4 and q.M < (p.M if not hasattr(p, "counts") else int(p.counts.max())):
+        rows = int(min(4096, max(8, rows * target_s / 2 / max(dt, 1e-3))))
+        q = oracle_sample(p, rows)
+        t = time.perf_counter()
+        oracle.gemm(q)
+        dt = time.perf_counter() - t
+    f = flops_of(q)
+    val = (algorithmic_bytes(q) / dt / 1e9) if unit == "GB/s" else f / dt / 1e12
+    return {"value": round(val, 6), "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"first {q.M} rows x all {q.N} columns x full K={q.K} of the workload, "
+                      f"{dt:.2f} s of fp64 OpenMP work"}
+
+
+def run_reference(args, rank, world, cfg):
+    import oracle
+
+    if rank != 0:
+        return None
+    p = make_problem(cfg)
+    metric, unit, _ = metric_of(cfg)
+    oracle.build()
+    rows = 16
+    q = oracle_sample(p, rows)
+    for _ in range(args.warmup if args.warmup < 3 else 3):
+        oracle.gemm(oracle_sample(p, 2))
+    times = []
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.gemm(q)
+        times.append(time.perf_counter() - t)
+        if time.perf_counter() - t_all > 150:
+            break
+    dt = statistics.mean(times)
+    val = (algorithmic_bytes(q) / dt / 1e9) if unit == "GB/s" else flops_of(q) / dt / 1e12
+    sample = f"first {q.M} rows x all {q.N} columns x full K={q.K} per step"
+    return {"impl": "reference", "metric": metric, "value": round(val, 6), "unit": unit, "n_gpus": world,
+            "steps": len(times), "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOADS[cfg]["desc"], "sample": sample},
+            "cpu_baseline": {"value": round(val, 6), "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(val, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=sorted(WORKLOADS), default="c2")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+    if "RANK" not in os.environ:
+        world = 1 if args.gpus == 1 else args.gpus
+        if world > 1:
+            ap.error("run --gpus N > 1 under torchrun (one process per GPU)")
+    if args.impl == "reference":
+        line = run_reference(args, rank, world, args.config)
+    else:
+        line = run_ours(args, rank, world, args.config)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

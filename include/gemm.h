@@ -65,8 +65,8 @@ typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_order_t;
  * Operands served (anything else returns GEMM_ERR_UNSUPPORTED):
  *   A : M x K, row-major, f16/bf16                 (K contiguous)
  *   B : K x N, col-major, same type as A, or S4     (K contiguous)
- *   U : (K/ga) x M, row-major, f16/bf16/f32        scale of A per (row, K-group)
- *   V : (K/gb) x N, row-major, f16/bf16/f32        scale of B per (K-group, column)
+ *   U : (K/ga) x M, row-major, f16/bf16            scale of A per (row, K-group)
+ *   V : (K/gb) x N, row-major, f16/bf16            scale of B per (K-group, column)
  *   C : M x N, row-major, same type as D
  *   D : M x N, row-major, f32/f16/bf16
  * A and B base addresses must be 16-byte aligned and their ld a multiple of

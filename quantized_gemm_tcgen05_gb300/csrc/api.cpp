@@ -203,40 +203,32 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
     CUtensorMap tx, ty;
     int rc;
     const bool dq = p.family == FAM_DQ;
+    const bool s4 = p.b_type == GEMM_S4;
     if (p.family == FAM_GROUPED) {
         rc = make_map(h, &tx, p.A, p.a_type, p.K, p.M, p.lda, 1, 0, 128);
         if (rc == GEMM_OK) rc = make_map(h, &ty, p.B, p.b_type, p.K, p.N, p.ldb, p.num_experts, p.b_bs, c.bn);
         kp.x3d = 0;
         kp.y3d = 1;
     } else if (c.swap) {
-        rc = make_map(h, &tx, p.B, p.b_type, p.K, p.N, p.ldb, 1, 0, 128);
+        rc = s4 ? make_map_s4(h, &tx, p.B, p.K, p.N, p.ldb, 128) : make_map(h, &tx, p.B, p.b_type, p.K, p.N, p.ldb, 1, 0, 128);
         if (rc == GEMM_OK) rc = make_map(h, &ty, p.A, p.a_type, p.K, p.M, p.lda, 1, 0, c.bn);
         kp.x3d = kp.y3d = 0;
     } else {
         rc = make_map(h, &tx, p.A, p.a_type, p.K, p.M, p.lda, p.batches, p.a_bs, 128);
-        if (rc == GEMM_OK) {
-            if (dq && p.b_type == GEMM_S4)
-                rc = make_map_s4(h, &ty, p.B, p.K, p.N, p.ldb, c.bn);
-            else
-                rc = make_map(h, &ty, p.B, p.b_type, p.K, p.N, p.ldb, p.batches, p.b_bs, c.bn);
-        }
+        if (rc == GEMM_OK)
+            rc = s4 ? make_map_s4(h, &ty, p.B, p.K, p.N, p.ldb, c.bn)
+                    : make_map(h, &ty, p.B, p.b_type, p.K, p.N, p.ldb, p.batches, p.b_bs, c.bn);
         kp.x3d = kp.y3d = p.batches > 1;
     }
     if (rc != GEMM_OK) return rc;
     if (dq) {
         DqParams& d = kp.dq;
+        d.K = p.K;
         d.out_bf16 = p.a_type == GEMM_BF16;
-        d.y_int4 = p.b_type == GEMM_S4;
-        d.y_scale = p.V;
-        d.y_scale_ld = p.ldv;
-        d.y_scale_type = p.v_type;
-        d.y_group = p.gb;
-        d.x_scale = p.U;
-        d.x_scale_ld = p.ldu;
-        d.x_scale_type = p.u_type;
-        d.x_group = p.ga;
-        d.y_rows = p.N;
-        d.x_rows = p.M;
+        OperandXform a_side{p.U, p.ldu, p.M, p.u_type, p.ga, 0, p.U != nullptr};
+        OperandXform b_side{p.V, p.ldv, p.N, p.v_type, p.gb, s4 ? 1 : 0, (p.V != nullptr || s4) ? 1 : 0};
+        d.x = c.swap ? b_side : a_side;
+        d.y = c.swap ? a_side : b_side;
         kp.stages = umma_dq_max_stages(c.bn);
         if (kp.stages < 2) return GEMM_ERR_NO_KERNEL;
         cudaError_t ce = launch_umma_dq_gemm(c.bn, tx, ty, kp, kp.sched.programs, st);
@@ -282,6 +274,34 @@ float measure(gemm_handle* h, const Problem& p, const Choice& c, const gemm_work
     return best[1] * 1000.0f;
 }
 
+// GEMM_FORCE_KERNEL="<family>_bn<N>[_swap]/<dp|streamk|splitk<S>>" (the
+// names gemm_last_choice prints) pins the kernel, for tests and sweeps.
+bool forced_kernel(const Problem& p, Choice* out) {
+    const char* f = getenv("GEMM_FORCE_KERNEL");
+    if (!f || !*f) return false;
+    const char* bn = strstr(f, "bn");
+    const char* slash = strchr(f, '/');
+    if (!bn || !slash) return false;
+    Choice c;
+    c.bn = atoi(bn + 2);
+    c.swap = strstr(f, "_swap") != nullptr && strstr(f, "_swap") < slash;
+    if (strncmp(slash + 1, "dp", 2) == 0) {
+        c.sched = SCHED_DP;
+    } else if (strncmp(slash + 1, "streamk", 7) == 0) {
+        c.sched = SCHED_STREAMK;
+    } else if (strncmp(slash + 1, "splitk", 6) == 0) {
+        c.sched = SCHED_SPLITK;
+        c.splits = atoi(slash + 7);
+    } else {
+        return false;
+    }
+    if (!(c.bn == 16 || c.bn == 32 || c.bn == 64 || c.bn == 128 || c.bn == 256)) return false;
+    if (c.swap && (p.family == FAM_GROUPED || p.batches != 1)) return false;
+    if (p.family == FAM_GROUPED) c.sched = SCHED_DP;
+    *out = c;
+    return true;
+}
+
 int dispatch_and_run(gemm_handle* h, const gemm_op_t* op, Problem& p, const gemm_workspace_t* ws, cudaStream_t st) {
     if (p.M == 0 || p.N == 0) {
         h->last_choice = "empty";
@@ -305,11 +325,12 @@ int dispatch_and_run(gemm_handle* h, const gemm_op_t* op, Problem& p, const gemm
         return launch_scale_c(e, p.batches, st) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
     Choice c;
-    bool have = false;
+    bool have = forced_kernel(p, &c);
+    if (have && !workspace_fits(h, p, c, ws)) return GEMM_ERR_WORKSPACE;
     const int forced_split = op->splitk > 1 ? op->splitk : h->force_splitk;
     const bool forced = forced_split > 1 || op->splitk == 1 || op->streamk != 0;
     const Key key = make_key(p);
-    if (!forced && op->dispatch != GEMM_DISPATCH_MEASURE) {
+    if (!have && !forced && op->dispatch != GEMM_DISPATCH_MEASURE) {
         auto it = h->cache.find(key);
         if (it != h->cache.end()) {
             c = it->second;
@@ -326,6 +347,7 @@ int dispatch_and_run(gemm_handle* h, const gemm_op_t* op, Problem& p, const gemm
             for (const Choice& cand : candidates(p, h->sm_count)) {
                 if (!workspace_fits(h, p, cand, ws)) continue;
                 float us = measure(h, p, cand, ws, st);
+                if (h->log) fprintf(stderr, "qgemm: measured %s: %.2f us\n", choice_name(p, cand).c_str(), us);
                 if (us > 0 && (best < 0 || us < best)) {
                     best = us;
                     c = cand;
@@ -347,6 +369,11 @@ int dispatch_and_run(gemm_handle* h, const gemm_op_t* op, Problem& p, const gemm
             if (c.sched != SCHED_DP && (op->splitk == 1 || c.sched == SCHED_STREAMK)) c.sched = SCHED_DP;
         }
         if (p.family == FAM_GROUPED) c.sched = SCHED_DP;
+        if (!workspace_fits(h, p, c, ws) && c.sched != SCHED_DP && !c.swap && c.bn > 128) {
+            Choice narrower = c;  // half-width tiles halve the partial-tile footprint
+            narrower.bn = 128;
+            if (workspace_fits(h, p, narrower, ws)) c = narrower;
+        }
         if (!workspace_fits(h, p, c, ws)) {
             if (forced) return GEMM_ERR_WORKSPACE;
             c.sched = SCHED_DP;  // automatic choices fall back to no split
@@ -414,7 +441,7 @@ int build_problem(gemm_handle* h, const gemm_op_t* op, float alpha, const void* 
         if (!Udesc || op->quant_a_group <= 0) return GEMM_ERR_INVALID_ARG;
         p.ga = op->quant_a_group;
         if (p.ga % 8 || p.K % p.ga) return GEMM_ERR_INVALID_ARG;
-        if (!(is16(Udesc->type) || Udesc->type == GEMM_F32)) return GEMM_ERR_UNSUPPORTED;
+        if (!is16(Udesc->type)) return GEMM_ERR_UNSUPPORTED;
         if ((rc = check_layout(Udesc, GEMM_ROW_MAJOR, p.K / p.ga, p.M))) return rc;
         if (Udesc->num != 1) return GEMM_ERR_UNSUPPORTED;
         p.U = U;
@@ -425,7 +452,7 @@ int build_problem(gemm_handle* h, const gemm_op_t* op, float alpha, const void* 
         if (!Vdesc || op->quant_b_group <= 0) return GEMM_ERR_INVALID_ARG;
         p.gb = op->quant_b_group;
         if (p.gb % 8 || p.K % p.gb) return GEMM_ERR_INVALID_ARG;
-        if (!(is16(Vdesc->type) || Vdesc->type == GEMM_F32)) return GEMM_ERR_UNSUPPORTED;
+        if (!is16(Vdesc->type)) return GEMM_ERR_UNSUPPORTED;
         if ((rc = check_layout(Vdesc, GEMM_ROW_MAJOR, p.K / p.gb, p.N))) return rc;
         if (Vdesc->num != 1) return GEMM_ERR_UNSUPPORTED;
         p.V = V;

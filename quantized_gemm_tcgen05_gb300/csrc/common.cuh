@@ -23,7 +23,7 @@ struct Guard {
     volatile uint32_t* abort;  // shared flag: once set, every role stops waiting
 };
 
-__device__ __noinline__ void record_timeout(const Guard& g, uint32_t site) {
+static __device__ __noinline__ void record_timeout(const Guard& g, uint32_t site) {
     *g.abort = 1u;
     if (g.status) {
         atomicExch(&g.status[1], site);
@@ -147,16 +147,67 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[W]) {
     }
 }
 
+// The C values one thread combines for one chunk, loaded before they are
+// needed so the epilogue does not wait on global-memory latency per row.
+template <int W>
+struct CChunk {
+    float v[W];
+};
+
+// Row-per-thread layout (non-swapped): iteration `it` of a thread covers tile
+// row ew*32 + it*(32/Q) + lane/Q and the 4 columns 4*(lane%Q) .. +3.
+template <int W>
+__device__ __forceinline__ void load_c_chunk(const EpiParams& e, const Unit& u, int ew, int lane, int col0,
+                                             CChunk<W>& cc) {
+    if (e.beta == 0.0f) return;
+    constexpr int Q = W / 4;
+    const int64_t boff_c = (int64_t)u.batch * e.c_bstride;
+    if (e.swap) {
+        const int64_t n = u.x_row0 + ew * 32 + lane;
+        const bool nok = n < e.N && ew * 32 + lane < u.x_rows;
+#pragma unroll
+        for (int j = 0; j < W; ++j) {
+            const int64_t m = u.y_row0 + col0 + j;
+            cc.v[j] = (nok && m < e.M) ? ld_elem(e.C, e.d_type, boff_c + m * e.ldc + n) : 0.0f;
+        }
+        return;
+    }
+    constexpr int ROWS_PER_IT = 32 / Q;
+#pragma unroll
+    for (int it = 0; it < Q; ++it) {
+        const int rr = it * ROWS_PER_IT + lane / Q;
+        const int j = lane % Q;
+        const int rt = ew * 32 + rr;
+        const int64_t m = u.x_row0 + rt;
+        const int64_t n0 = u.y_row0 + col0 + 4 * j;
+        float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (rt < u.x_rows && m < e.M && n0 < e.N) {
+            const int64_t ci = boff_c + m * e.ldc + n0;
+            if (e.vec_ok && n0 + 3 < e.N) {
+                c = ld4(e.C, e.d_type, ci);
+            } else {
+                c.x = ld_elem(e.C, e.d_type, ci);
+                if (n0 + 1 < e.N) c.y = ld_elem(e.C, e.d_type, ci + 1);
+                if (n0 + 2 < e.N) c.z = ld_elem(e.C, e.d_type, ci + 2);
+                if (n0 + 3 < e.N) c.w = ld_elem(e.C, e.d_type, ci + 3);
+            }
+        }
+        cc.v[4 * it] = c.x;
+        cc.v[4 * it + 1] = c.y;
+        cc.v[4 * it + 2] = c.z;
+        cc.v[4 * it + 3] = c.w;
+    }
+}
+
 // Store one chunk of W accumulator columns held by this thread for tile row
-// `r` (= ew*32 + lane) through the epilogue.  `staging` is this warp's private
-// 32 x W fp32 buffer (swizzled by 16-byte quads) used to turn the row-per-
-// thread TMEM layout into row-contiguous global stores.
+// r = ew*32 + lane, combined with the prefetched C values.  `staging` is this
+// warp's private 32 x W fp32 buffer (swizzled by 16-byte quads) that turns the
+// row-per-thread TMEM layout into row-contiguous global stores.
 template <int W>
 __device__ __forceinline__ void store_chunk(const EpiParams& e, const Unit& u, int ew, int lane, int col0,
-                                            const float (&v)[W], float4* staging) {
+                                            const float (&v)[W], const CChunk<W>& cc, float4* staging) {
     constexpr int Q = W / 4;
     const int64_t boff_d = (int64_t)u.batch * e.d_bstride;
-    const int64_t boff_c = (int64_t)u.batch * e.c_bstride;
     if (e.swap) {
         // tile row -> output column n; tile column -> output row m.  Lanes
         // hold consecutive n, so each store instruction is row-contiguous.
@@ -165,22 +216,17 @@ __device__ __forceinline__ void store_chunk(const EpiParams& e, const Unit& u, i
 #pragma unroll
         for (int j = 0; j < W; ++j) {
             const int64_t m = u.y_row0 + col0 + j;
-            if (m < e.M) {
-                float c = e.beta != 0.0f ? ld_elem(e.C, e.d_type, boff_c + m * e.ldc + n) : 0.0f;
-                st_elem(e.D, e.d_type, boff_d + m * e.ldd + n, epi_value(e, v[j], c));
-            }
+            if (m < e.M) st_elem(e.D, e.d_type, boff_d + m * e.ldd + n, epi_value(e, v[j], cc.v[j]));
         }
         return;
     }
-    // row r of the tile holds W consecutive columns: stage them, then let
-    // each group of Q lanes write one row segment.
 #pragma unroll
     for (int j = 0; j < Q; ++j)
         staging[lane * Q + (j ^ (lane & (Q - 1)))] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     __syncwarp();
     constexpr int ROWS_PER_IT = 32 / Q;
 #pragma unroll
-    for (int it = 0; it < 32 / ROWS_PER_IT; ++it) {
+    for (int it = 0; it < Q; ++it) {
         const int rr = it * ROWS_PER_IT + lane / Q;  // row within this warp's 32
         const int j = lane % Q;
         const float4 a = staging[rr * Q + (j ^ (rr & (Q - 1)))];
@@ -189,18 +235,13 @@ __device__ __forceinline__ void store_chunk(const EpiParams& e, const Unit& u, i
         const int64_t n0 = u.y_row0 + col0 + 4 * j;
         if (rt >= u.x_rows || m >= e.M || n0 >= e.N) continue;
         const int64_t di = boff_d + m * e.ldd + n0;
-        const int64_t ci = boff_c + m * e.ldc + n0;
+        const float4 o = make_float4(epi_value(e, a.x, cc.v[4 * it]), epi_value(e, a.y, cc.v[4 * it + 1]),
+                                     epi_value(e, a.z, cc.v[4 * it + 2]), epi_value(e, a.w, cc.v[4 * it + 3]));
         if (e.vec_ok && n0 + 3 < e.N) {
-            float4 c = e.beta != 0.0f ? ld4(e.C, e.d_type, ci) : make_float4(0.f, 0.f, 0.f, 0.f);
-            float4 o = make_float4(epi_value(e, a.x, c.x), epi_value(e, a.y, c.y), epi_value(e, a.z, c.z),
-                                   epi_value(e, a.w, c.w));
             st4(e.D, e.d_type, di, o);
         } else {
-            const float av[4] = {a.x, a.y, a.z, a.w};
-            for (int q = 0; q < 4 && n0 + q < e.N; ++q) {
-                float c = e.beta != 0.0f ? ld_elem(e.C, e.d_type, ci + q) : 0.0f;
-                st_elem(e.D, e.d_type, di + q, epi_value(e, av[q], c));
-            }
+            const float ov[4] = {o.x, o.y, o.z, o.w};
+            for (int q = 0; q < 4 && n0 + q < e.N; ++q) st_elem(e.D, e.d_type, di + q, ov[q]);
         }
     }
     __syncwarp();
@@ -238,15 +279,32 @@ __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uin
         tc_fence_after_sync();
         const uint32_t tbase = tmem_base + (uint32_t)(buf * BN) + ((uint32_t)(ew * 32) << 16);
         if (u.mode == UNIT_FULL) {
+            // C for chunk c+1 is fetched while chunk c is stored (two buffers,
+            // alternated by a two-step loop so they stay in registers)
+            CChunk<CK::W> c0, c1;
+            load_c_chunk<CK::W>(P.epi, u, ew, lane, 0, c0);
 #pragma unroll 1
-            for (int c = 0; c < CK::N; ++c) {
-                float v[CK::W];
-                tmem_load_chunk<CK::W>(tbase + c * CK::W, v);
-                if (c == CK::N - 1) {
-                    tc_fence_before_sync();
-                    mbar_arrive(&tempty[buf]);
+            for (int c = 0; c < CK::N; c += 2) {
+                if (c + 1 < CK::N) load_c_chunk<CK::W>(P.epi, u, ew, lane, (c + 1) * CK::W, c1);
+                {
+                    float v[CK::W];
+                    tmem_load_chunk<CK::W>(tbase + c * CK::W, v);
+                    if (c == CK::N - 1) {
+                        tc_fence_before_sync();
+                        mbar_arrive(&tempty[buf]);
+                    }
+                    store_chunk<CK::W>(P.epi, u, ew, lane, c * CK::W, v, c0, staging);
                 }
-                store_chunk<CK::W>(P.epi, u, ew, lane, c * CK::W, v, staging);
+                if (c + 1 < CK::N) {
+                    if (c + 2 < CK::N) load_c_chunk<CK::W>(P.epi, u, ew, lane, (c + 2) * CK::W, c0);
+                    float v[CK::W];
+                    tmem_load_chunk<CK::W>(tbase + (c + 1) * CK::W, v);
+                    if (c + 1 == CK::N - 1) {
+                        tc_fence_before_sync();
+                        mbar_arrive(&tempty[buf]);
+                    }
+                    store_chunk<CK::W>(P.epi, u, ew, lane, (c + 1) * CK::W, v, c1, staging);
+                }
             }
             continue;
         }
@@ -275,22 +333,41 @@ __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uin
         __threadfence();
 #pragma unroll 1
         for (int c = 0; c < CK::N; ++c) {
+            CChunk<CK::W> cc;
+            load_c_chunk<CK::W>(P.epi, u, ew, lane, c * CK::W, cc);
             float v[CK::W];
 #pragma unroll
             for (int i = 0; i < CK::W; ++i) v[i] = 0.0f;
+            // contributors in K order, two at a time so their loads overlap
 #pragma unroll 1
-            for (int q = 0; q < u.ncontrib; ++q) {
-                const int64_t slot = partial_slot(P.sched, u.tile, q);
+            for (int q0 = 0; q0 < u.ncontrib; q0 += 2) {
+                const bool two = q0 + 1 < u.ncontrib;
+                const int64_t s0 = partial_slot(P.sched, u.tile, q0);
+                const int64_t s1 = two ? partial_slot(P.sched, u.tile, q0 + 1) : s0;
+                float4 p0[CK::Q], p1[CK::Q];
 #pragma unroll
                 for (int j = 0; j < CK::Q; ++j) {
-                    const float4 p = __ldcg(partial_quad<BN>(P.partials, slot, c, j, r));
-                    v[4 * j] += p.x;
-                    v[4 * j + 1] += p.y;
-                    v[4 * j + 2] += p.z;
-                    v[4 * j + 3] += p.w;
+                    p0[j] = __ldcg(partial_quad<BN>(P.partials, s0, c, j, r));
+                    p1[j] = __ldcg(partial_quad<BN>(P.partials, s1, c, j, r));
+                }
+#pragma unroll
+                for (int j = 0; j < CK::Q; ++j) {
+                    v[4 * j] += p0[j].x;
+                    v[4 * j + 1] += p0[j].y;
+                    v[4 * j + 2] += p0[j].z;
+                    v[4 * j + 3] += p0[j].w;
+                }
+                if (two) {
+#pragma unroll
+                    for (int j = 0; j < CK::Q; ++j) {
+                        v[4 * j] += p1[j].x;
+                        v[4 * j + 1] += p1[j].y;
+                        v[4 * j + 2] += p1[j].z;
+                        v[4 * j + 3] += p1[j].w;
+                    }
                 }
             }
-            store_chunk<CK::W>(P.epi, u, ew, lane, c * CK::W, v, staging);
+            store_chunk<CK::W>(P.epi, u, ew, lane, c * CK::W, v, cc, staging);
         }
     }
 }

@@ -113,7 +113,7 @@ static int32_t swap_bn(int64_t M) {
 }
 
 static bool swap_allowed(const Problem& p) {
-    return p.family == FAM_DENSE && p.batches == 1 && p.M <= 128;
+    return (p.family == FAM_DENSE || p.family == FAM_DQ) && p.batches == 1 && p.M <= 128;
 }
 
 std::vector<Choice> candidates(const Problem& p, int sm_count) {
@@ -144,6 +144,7 @@ std::vector<Choice> candidates(const Problem& p, int sm_count) {
     if (p.family == FAM_DQ) {
         for (int32_t bn : {64, 128, 256})
             if (bn == 64 || p.N > bn / 2) add_scheds(bn, 0);
+        if (swap_allowed(p)) add_scheds(swap_bn(p.M), 1);
         return out;
     }
     add_scheds(128, 0);

@@ -38,22 +38,25 @@ struct EpiParams {
     int32_t vec_ok;    // C/D bases and ld allow 16-byte vector access
 };
 
-// Group-wise scale / dequantisation applied to the shared-memory operands
-// before the tensor core reads them (the "GroupIter" role of the pages).
+// Group-wise scaling / int4 dequantisation of one shared-memory operand
+// before the tensor core reads it (the role of the scale operands U/V that
+// advance at K-group boundaries).  The operand's value at (row r, k) becomes
+// RN(x[r][k] * scale[k / group][r]) in the MMA input type, with x the int4
+// nibble or the stored 16-bit value.
+struct OperandXform {
+    const void* scale;   // [K/group][rows], rows contiguous, or NULL (no scaling)
+    int64_t scale_ld;    // elements
+    int64_t rows;        // valid rows of the operand (scale reads are bounded by it)
+    int32_t scale_type;  // DT_F16 / DT_BF16
+    int32_t group;       // group size along K (multiple of 8)
+    int32_t int4;        // operand is packed int4 (raw tile rows of 32 bytes)
+    int32_t active;      // any transform at all
+};
+
 struct DqParams {
-    // Y operand (UMMA N side, "B" of a non-swapped GEMM)
-    const void* y_scale;     // [K/gy][y_rows] scales, y_rows contiguous, or NULL
-    int64_t y_scale_ld;      // elements
-    int32_t y_scale_type;    // DT_F16 / DT_BF16 / DT_F32
-    int32_t y_group;         // group size along K
-    int32_t y_int4;          // Y is packed int4 (raw tile is BN x 32 bytes)
-    // X operand (UMMA M side, "A" of a non-swapped GEMM)
-    const void* x_scale;     // [K/gx][x_rows] or NULL
-    int64_t x_scale_ld;
-    int32_t x_scale_type;
-    int32_t x_group;
-    int32_t out_bf16;        // the rounded operand type: 1 bf16, 0 f16
-    int64_t y_rows, x_rows;  // rows of the scaled operands (for bounds)
+    OperandXform x, y;   // X: UMMA M side (128-row tiles), Y: UMMA N side
+    int64_t K;
+    int32_t out_bf16;    // rounded operand type: 1 bf16, 0 f16
 };
 
 struct GemmKernelParams {
