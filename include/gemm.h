@@ -69,9 +69,10 @@ typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_order_t;
  *   V : (K/gb) x N, row-major, f16/bf16            scale of B per (K-group, column)
  *   C : M x N, row-major, same type as D
  *   D : M x N, row-major, f32/f16/bf16
- * A and B base addresses must be 16-byte aligned and their ld a multiple of
- * 16 bytes (they are read by the tensor-memory accelerator); C and D may have
- * any ld >= N and element alignment.
+ * A, B, U and V base addresses must be 16-byte aligned and their ld a
+ * multiple of 16 bytes (they are read by the tensor-memory accelerator); C
+ * and D may have any ld >= N and element alignment (16-byte aligned ones are
+ * moved through shared memory by TMA, others element by element).
  */
 typedef struct {
     int32_t type;          /* gemm_dtype_t  */
@@ -97,8 +98,8 @@ enum {
 typedef struct {
     int32_t dispatch;      /* GEMM_DISPATCH_*                                        */
     int32_t epilogue;      /* 0: alpha/beta/cast (the only epilogue served)          */
-    int32_t quant_a_group; /* 0: no U; else group size of U along K (multiple of 8)  */
-    int32_t quant_b_group; /* 0: no V; else group size of V along K (multiple of 8)  */
+    int32_t quant_a_group; /* 0: no U; else U's group size along K: 8, 16, 32 or a multiple of 64 */
+    int32_t quant_b_group; /* 0: no V; else V's group size along K: 8, 16, 32 or a multiple of 64 */
     int32_t splitk;        /* 0: automatic; 1: unsplit; S > 1: force S K-slices       */
     int32_t streamk;       /* 0: automatic; 1: force stream-K; -1: never stream-K     */
 } gemm_op_t;

@@ -166,6 +166,41 @@ int make_map_s4(gemm_handle* h, CUtensorMap* m, const void* ptr, int64_t K, int6
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+// Tensor map over a [batches][M][N] row-major C or D with 32 x 32 boxes in
+// the swizzled layout the TMA epilogue reads and writes (64-byte rows for
+// 16-bit types, 128-byte rows for fp32).
+int make_map_cd(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t type, int64_t M, int64_t N, int64_t ld,
+                int32_t batches, int64_t bstride) {
+    const int64_t es = type == GEMM_F32 ? 4 : 2;
+    CUtensorMapDataType dt = type == GEMM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                              : (type == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+    cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)batches};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld * es), (cuuint64_t)(bstride * es)};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const cuuint32_t rank = batches > 1 ? 3 : 2;
+    CUresult r = h->encode(m, dt, rank, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           es == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// Tensor map over a [groups][cols] row-major scale matrix (U or V): each
+// K-step copies box_rows group rows x box_cols columns into its stage.
+int make_map_scale(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t type, int64_t groups, int64_t cols,
+                   int64_t ld, int32_t box_cols, int32_t box_rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)groups};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUtensorMapDataType dt = type == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = h->encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
 int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_workspace_t* ws, cudaStream_t st) {
     GemmKernelParams kp;
     memset(&kp, 0, sizeof kp);
@@ -200,7 +235,10 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
     kp.status = h->status;
     kp.timeout_ns = h->timeout_ns;
 
-    CUtensorMap tx, ty;
+    GemmMaps maps;
+    memset(&maps, 0, sizeof maps);
+    CUtensorMap& tx = maps.x;
+    CUtensorMap& ty = maps.y;
     int rc;
     const bool dq = p.family == FAM_DQ;
     const bool s4 = p.b_type == GEMM_S4;
@@ -221,22 +259,68 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
         kp.x3d = kp.y3d = p.batches > 1;
     }
     if (rc != GEMM_OK) return rc;
+    // TMA epilogue: C / D through shared memory when their layout allows it
+    {
+        const int64_t es = p.d_type == GEMM_F32 ? 4 : 2;
+        auto ok16 = [&](const void* ptr, int64_t ld, int64_t bs) {
+            return aligned16(ptr) && (ld * es) % 16 == 0 && (p.batches == 1 || (bs * es) % 16 == 0);
+        };
+        const char* et = getenv("GEMM_EPI_TMA");
+        const bool allowed = !(et && et[0] == '0');
+        e.tma = allowed && !c.swap && p.family != FAM_GROUPED && c.bn >= 32 && ok16(p.D, p.ldd, p.d_bs) &&
+                (e.C == nullptr || ok16(p.C, p.ldc, p.c_bs));
+        if (e.tma) {
+            e.ncb = es == 2 ? 4 : 2;
+            rc = make_map_cd(h, &maps.d, p.D, p.d_type, p.M, p.N, p.ldd, p.batches, p.d_bs);
+            if (rc == GEMM_OK && e.C) rc = make_map_cd(h, &maps.c, p.C, p.d_type, p.M, p.N, p.ldc, p.batches, p.c_bs);
+            if (rc != GEMM_OK) return rc;
+        }
+    }
     if (dq) {
         DqParams& d = kp.dq;
         d.K = p.K;
         d.out_bf16 = p.a_type == GEMM_BF16;
-        OperandXform a_side{p.U, p.ldu, p.M, p.u_type, p.ga, 0, p.U != nullptr};
-        OperandXform b_side{p.V, p.ldv, p.N, p.v_type, p.gb, s4 ? 1 : 0, (p.V != nullptr || s4) ? 1 : 0};
+        auto xform = [](const void* scale, int32_t type, int32_t group, int32_t int4) {
+            OperandXform o;
+            o.has_scale = scale != nullptr;
+            o.scale_type = type;
+            o.group = scale ? group : 64;
+            o.sc_rows = scale ? (group >= 64 ? 1 : 64 / group) : 0;
+            o.int4 = int4;
+            o.active = scale != nullptr || int4;
+            return o;
+        };
+        const OperandXform a_side = xform(p.U, p.u_type, p.ga, 0);
+        const OperandXform b_side = xform(p.V, p.v_type, p.gb, s4 ? 1 : 0);
         d.x = c.swap ? b_side : a_side;
         d.y = c.swap ? a_side : b_side;
+        // scale rows: X side tiles are 128 rows, Y side tiles are BN rows
+        const void* xs_ptr = c.swap ? p.V : p.U;
+        const void* ys_ptr = c.swap ? p.U : p.V;
+        if (xs_ptr) {
+            const bool v = c.swap;
+            rc = make_map_scale(h, &maps.xs, xs_ptr, v ? p.v_type : p.u_type, p.K / (v ? p.gb : p.ga), v ? p.N : p.M,
+                                v ? p.ldv : p.ldu, 128, d.x.sc_rows);
+            if (rc != GEMM_OK) return rc;
+        }
+        if (ys_ptr) {
+            const bool v = !c.swap;
+            rc = make_map_scale(h, &maps.ys, ys_ptr, v ? p.v_type : p.u_type, p.K / (v ? p.gb : p.ga), v ? p.N : p.M,
+                                v ? p.ldv : p.ldu, c.bn, d.y.sc_rows);
+            if (rc != GEMM_OK) return rc;
+        }
         kp.stages = umma_dq_max_stages(c.bn);
         if (kp.stages < 2) return GEMM_ERR_NO_KERNEL;
-        cudaError_t ce = launch_umma_dq_gemm(c.bn, tx, ty, kp, kp.sched.programs, st);
+        cudaError_t ce = launch_umma_dq_gemm(c.bn, maps, kp, kp.sched.programs, st);
         return ce == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
     kp.stages = umma_max_stages(c.bn);
     if (kp.stages < 2) return GEMM_ERR_NO_KERNEL;
-    cudaError_t ce = launch_umma_gemm(c.bn, tx, ty, kp, kp.sched.programs, st);
+    if (const char* fs = getenv("GEMM_STAGES")) {  // ring depth override for tuning sweeps
+        const int want = atoi(fs);
+        if (want >= 2 && want < kp.stages) kp.stages = want;
+    }
+    cudaError_t ce = launch_umma_gemm(c.bn, maps, kp, kp.sched.programs, st);
     return ce == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -440,10 +524,11 @@ int build_problem(gemm_handle* h, const gemm_op_t* op, float alpha, const void* 
     if (U) {
         if (!Udesc || op->quant_a_group <= 0) return GEMM_ERR_INVALID_ARG;
         p.ga = op->quant_a_group;
-        if (p.ga % 8 || p.K % p.ga) return GEMM_ERR_INVALID_ARG;
+        if (p.ga < 8 || p.K % p.ga || (p.ga % 64 && 64 % p.ga)) return GEMM_ERR_INVALID_ARG;
         if (!is16(Udesc->type)) return GEMM_ERR_UNSUPPORTED;
         if ((rc = check_layout(Udesc, GEMM_ROW_MAJOR, p.K / p.ga, p.M))) return rc;
         if (Udesc->num != 1) return GEMM_ERR_UNSUPPORTED;
+        if (!aligned16(U) || (Udesc->ld * 2) % 16) return GEMM_ERR_INVALID_ARG;  // copied by TMA
         p.U = U;
         p.ldu = Udesc->ld;
         p.u_type = Udesc->type;
@@ -451,10 +536,11 @@ int build_problem(gemm_handle* h, const gemm_op_t* op, float alpha, const void* 
     if (V) {
         if (!Vdesc || op->quant_b_group <= 0) return GEMM_ERR_INVALID_ARG;
         p.gb = op->quant_b_group;
-        if (p.gb % 8 || p.K % p.gb) return GEMM_ERR_INVALID_ARG;
+        if (p.gb < 8 || p.K % p.gb || (p.gb % 64 && 64 % p.gb)) return GEMM_ERR_INVALID_ARG;
         if (!is16(Vdesc->type)) return GEMM_ERR_UNSUPPORTED;
         if ((rc = check_layout(Vdesc, GEMM_ROW_MAJOR, p.K / p.gb, p.N))) return rc;
         if (Vdesc->num != 1) return GEMM_ERR_UNSUPPORTED;
+        if (!aligned16(V) || (Vdesc->ld * 2) % 16) return GEMM_ERR_INVALID_ARG;  // copied by TMA
         p.V = V;
         p.ldv = Vdesc->ld;
         p.v_type = Vdesc->type;

@@ -14,6 +14,10 @@ namespace qg {
 constexpr int BM = 128;  // UMMA M: rows of the X operand per tile (TMEM lanes)
 constexpr int BK = 64;   // K per pipeline stage: one 128-byte swizzle row of 16-bit values
 constexpr int UMMA_K = 16;
+// Shared memory the epilogue owns: 16 KB of staging (register path) or the
+// per-warp C/D tile buffers (TMA path), whichever the launch uses.
+constexpr uint32_t EPI_SMEM_BYTES = 32 * 1024;
+constexpr int EPI_CBARS = 16;  // 4 epilogue warps x up to 4 buffers
 
 // ---- bounded waits -------------------------------------------------------------
 
@@ -279,32 +283,18 @@ __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uin
         tc_fence_after_sync();
         const uint32_t tbase = tmem_base + (uint32_t)(buf * BN) + ((uint32_t)(ew * 32) << 16);
         if (u.mode == UNIT_FULL) {
-            // C for chunk c+1 is fetched while chunk c is stored (two buffers,
-            // alternated by a two-step loop so they stay in registers)
-            CChunk<CK::W> c0, c1;
-            load_c_chunk<CK::W>(P.epi, u, ew, lane, 0, c0);
+            // C of a chunk is requested before its TMEM load so the two overlap
 #pragma unroll 1
-            for (int c = 0; c < CK::N; c += 2) {
-                if (c + 1 < CK::N) load_c_chunk<CK::W>(P.epi, u, ew, lane, (c + 1) * CK::W, c1);
-                {
-                    float v[CK::W];
-                    tmem_load_chunk<CK::W>(tbase + c * CK::W, v);
-                    if (c == CK::N - 1) {
-                        tc_fence_before_sync();
-                        mbar_arrive(&tempty[buf]);
-                    }
-                    store_chunk<CK::W>(P.epi, u, ew, lane, c * CK::W, v, c0, staging);
+            for (int c = 0; c < CK::N; ++c) {
+                CChunk<CK::W> cc;
+                load_c_chunk<CK::W>(P.epi, u, ew, lane, c * CK::W, cc);
+                float v[CK::W];
+                tmem_load_chunk<CK::W>(tbase + c * CK::W, v);
+                if (c == CK::N - 1) {
+                    tc_fence_before_sync();
+                    mbar_arrive(&tempty[buf]);
                 }
-                if (c + 1 < CK::N) {
-                    if (c + 2 < CK::N) load_c_chunk<CK::W>(P.epi, u, ew, lane, (c + 2) * CK::W, c0);
-                    float v[CK::W];
-                    tmem_load_chunk<CK::W>(tbase + (c + 1) * CK::W, v);
-                    if (c + 1 == CK::N - 1) {
-                        tc_fence_before_sync();
-                        mbar_arrive(&tempty[buf]);
-                    }
-                    store_chunk<CK::W>(P.epi, u, ew, lane, (c + 1) * CK::W, v, c1, staging);
-                }
+                store_chunk<CK::W>(P.epi, u, ew, lane, c * CK::W, v, cc, staging);
             }
             continue;
         }
@@ -370,6 +360,274 @@ __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uin
             store_chunk<CK::W>(P.epi, u, ew, lane, c * CK::W, v, cc, staging);
         }
     }
+}
+
+// Position in the per-warp stream of (unit, chunk) pairs, used to fetch C
+// ahead of the chunk being stored, across unit boundaries.
+struct ChunkStream {
+    WorkIter w;
+    Unit u;
+    int c;
+    bool valid;
+    __device__ __forceinline__ void init(const SchedParams& s, int pid, int bn) {
+        w.init(s, pid);
+        c = 0;
+        valid = w.next(s, pid, BM, bn, u);
+    }
+    __device__ __forceinline__ void advance(const SchedParams& s, int pid, int bn, int nch) {
+        if (++c == nch) {
+            c = 0;
+            valid = w.next(s, pid, BM, bn, u);
+        }
+    }
+};
+
+// TMA epilogue (non-swapped, non-grouped, 16-byte aligned C and D): every
+// epilogue warp owns `ncb` shared-memory buffers holding a 32-row x 32-column
+// slab of C / D in the TMA swizzled layout (64-byte rows for 16-bit types,
+// SWIZZLE_64B; 128-byte rows for fp32, SWIZZLE_128B).  C slabs are loaded
+// ncb-1 chunks ahead of use -- across unit boundaries, so they arrive while
+// the tensor core still works on the tile -- and each finished D slab is
+// written back in place and stored with one TMA store.
+template <int BN>
+__device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, const CUtensorMap* tmD,
+                             uint32_t tmem_base, uint64_t* tfull, uint64_t* tempty, uint8_t* ebuf_all,
+                             uint64_t* cbar_all, volatile uint32_t* bcast, const Guard& g) {
+    constexpr int W = 32;
+    constexpr int NCH = BN / W;
+    const EpiParams& e = P.epi;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int ew = warp % 4;
+    const int r = ew * 32 + lane;
+    const bool f32 = e.d_type == DT_F32;
+    const bool bf16 = e.d_type == DT_BF16;
+    const uint32_t buf_bytes = 32u * W * (f32 ? 4u : 2u);
+    const int ncb = e.ncb;
+    uint8_t* ebuf = ebuf_all + (size_t)ew * ncb * buf_bytes;
+    uint64_t* cbar = cbar_all + ew * 4;
+    const bool use_c = e.beta != 0.0f;
+    const int pid = blockIdx.x;
+
+    auto slab_x = [&](const Unit& u, int c) { return (int32_t)(u.y_row0 + c * W); };
+    auto slab_y = [&](const Unit& u) { return (int32_t)(u.x_row0 + ew * 32); };
+
+    // Store bookkeeping (lane 0): stores are numbered as they are committed;
+    // a buffer may be rewritten once every store up to its last one has read
+    // its source, i.e. once at most nstores - last_store[b] are still reading.
+    uint32_t nstores = 0;
+    uint32_t last_store[4] = {0, 0, 0, 0};
+    auto wait_buffer_read = [&](int b) {
+        const uint32_t newer = nstores - last_store[b];
+        if (newer == 0)
+            bulk_wait_group_read<0>();
+        else if (newer == 1)
+            bulk_wait_group_read<1>();
+        else if (newer == 2)
+            bulk_wait_group_read<2>();
+        else if (newer == 3)
+            bulk_wait_group_read<3>();
+        else  // four or more newer stores: waiting for all but the newest four suffices
+            bulk_wait_group_read<4>();
+    };
+
+    ChunkStream pre;
+    pre.init(P.sched, pid, BN);
+    uint32_t ppos = 0, gpos = 0;
+    auto issue_c = [&]() {
+        const int b = ppos % ncb;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&cbar[b], buf_bytes);
+            if (P.x3d)
+                tma_load_3d(ebuf + b * buf_bytes, tmC, &cbar[b], slab_x(pre.u, pre.c), slab_y(pre.u), pre.u.batch);
+            else
+                tma_load_2d(ebuf + b * buf_bytes, tmC, &cbar[b], slab_x(pre.u, pre.c), slab_y(pre.u));
+        }
+        pre.advance(P.sched, pid, BN, NCH);
+        ++ppos;
+    };
+    if (use_c)
+        for (int i = 0; i < ncb - 1 && pre.valid; ++i) issue_c();
+
+    // Combine chunk `c` of unit `u` (values v) with C and store it; when
+    // `store` is false the chunk's C slab is only consumed.
+    bool ok = true;
+    auto finish_chunk = [&](const Unit& u, int c, const float(&v)[W], bool store) {
+        const int b = gpos % ncb;
+        uint8_t* buf = ebuf + b * buf_bytes;
+        if (use_c) {
+            if (!wait_bar(&cbar[b], (gpos / ncb) & 1u, g, SITE_EPI_TMEM_FULL)) {
+                ok = false;
+                return;
+            }
+        } else {
+            if (lane == 0) wait_buffer_read(b);  // its previous store has read it
+            __syncwarp();
+        }
+        if (store) {
+            if (f32) {
+                uint8_t* row = buf + lane * 128;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    float4* pp = reinterpret_cast<float4*>(row + ((q ^ (lane & 7)) << 4));
+                    const float4 cv = use_c ? *pp : make_float4(0.f, 0.f, 0.f, 0.f);
+                    *pp = make_float4(epi_value(e, v[4 * q], cv.x), epi_value(e, v[4 * q + 1], cv.y),
+                                      epi_value(e, v[4 * q + 2], cv.z), epi_value(e, v[4 * q + 3], cv.w));
+                }
+            } else {
+                uint8_t* row = buf + lane * 64;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4* pp = reinterpret_cast<uint4*>(row + ((q ^ ((lane >> 1) & 3)) << 4));
+                    float cv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    if (use_c) {
+                        const uint4 in = *pp;
+                        const uint32_t iw[4] = {in.x, in.y, in.z, in.w};
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const float2 f = bf16 ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&iw[t]))
+                                                  : __half22float2(*reinterpret_cast<const __half2*>(&iw[t]));
+                            cv[2 * t] = f.x;
+                            cv[2 * t + 1] = f.y;
+                        }
+                    }
+                    uint32_t ow[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const float a = epi_value(e, v[8 * q + 2 * t], cv[2 * t]);
+                        const float b2 = epi_value(e, v[8 * q + 2 * t + 1], cv[2 * t + 1]);
+                        if (bf16) {
+                            __nv_bfloat162 h = __floats2bfloat162_rn(a, b2);
+                            ow[t] = *reinterpret_cast<uint32_t*>(&h);
+                        } else {
+                            __half2 h = __floats2half2_rn(a, b2);
+                            ow[t] = *reinterpret_cast<uint32_t*>(&h);
+                        }
+                    }
+                    *pp = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                }
+            }
+            fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (store && lane == 0) {
+            if (P.x3d)
+                tma_store_3d(tmD, buf, slab_x(u, c), slab_y(u), u.batch);
+            else
+                tma_store_2d(tmD, buf, slab_x(u, c), slab_y(u));
+            bulk_commit_group();
+            last_store[b] = ++nstores;
+        }
+        ++gpos;
+        if (use_c && pre.valid) {
+            if (lane == 0) wait_buffer_read(ppos % ncb);  // the next slab's buffer is free
+            __syncwarp();
+            issue_c();
+        }
+    };
+
+    WorkIter w;
+    w.init(P.sched, pid);
+    Unit u;
+    uint32_t acc_it = 0;
+    while (ok && w.next(P.sched, pid, BM, BN, u)) {
+        const int buf = acc_it & 1;
+        const uint32_t aph = (acc_it >> 1) & 1;
+        ++acc_it;
+        if (!wait_bar(&tfull[buf], aph, g, SITE_EPI_TMEM_FULL)) break;
+        tc_fence_after_sync();
+        const uint32_t tbase = tmem_base + (uint32_t)(buf * BN) + ((uint32_t)(ew * 32) << 16);
+        if (u.mode == UNIT_FULL) {
+#pragma unroll 1
+            for (int c = 0; c < NCH && ok; ++c) {
+                float v[W];
+                tmem_load_chunk<W>(tbase + c * W, v);
+                if (c == NCH - 1) {
+                    tc_fence_before_sync();
+                    mbar_arrive(&tempty[buf]);
+                }
+                finish_chunk(u, c, v, true);
+            }
+            continue;
+        }
+#pragma unroll 1
+        for (int c = 0; c < NCH; ++c) {
+            float v[W];
+            tmem_load_chunk<W>(tbase + c * W, v);
+#pragma unroll
+            for (int j = 0; j < W / 4; ++j)
+                *partial_quad<BN>(P.partials, u.slot, c, j, r) =
+                    make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
+        tc_fence_before_sync();
+        mbar_arrive(&tempty[buf]);
+        __threadfence();
+        epi_bar_sync();
+        if (threadIdx.x == 64) {
+            const int old = atomicAdd(&P.counters[u.tile], 1);
+            const bool last = (old == u.ncontrib - 1);
+            if (last) atomicExch(&P.counters[u.tile], 0);
+            *bcast = last ? 1u : 0u;
+        }
+        epi_bar_sync();
+        const bool last = *bcast != 0u;
+        if (last) __threadfence();
+#pragma unroll 1
+        for (int c = 0; c < NCH && ok; ++c) {
+            float v[W];
+#pragma unroll
+            for (int i = 0; i < W; ++i) v[i] = 0.0f;
+            if (last) {
+#pragma unroll 1
+                for (int q0 = 0; q0 < u.ncontrib; q0 += 2) {
+                    const bool two = q0 + 1 < u.ncontrib;
+                    const int64_t s0 = partial_slot(P.sched, u.tile, q0);
+                    const int64_t s1 = two ? partial_slot(P.sched, u.tile, q0 + 1) : s0;
+                    float4 p0[W / 4], p1[W / 4];
+#pragma unroll
+                    for (int j = 0; j < W / 4; ++j) {
+                        p0[j] = __ldcg(partial_quad<BN>(P.partials, s0, c, j, r));
+                        p1[j] = __ldcg(partial_quad<BN>(P.partials, s1, c, j, r));
+                    }
+#pragma unroll
+                    for (int j = 0; j < W / 4; ++j) {
+                        v[4 * j] += p0[j].x;
+                        v[4 * j + 1] += p0[j].y;
+                        v[4 * j + 2] += p0[j].z;
+                        v[4 * j + 3] += p0[j].w;
+                    }
+                    if (two) {
+#pragma unroll
+                        for (int j = 0; j < W / 4; ++j) {
+                            v[4 * j] += p1[j].x;
+                            v[4 * j + 1] += p1[j].y;
+                            v[4 * j + 2] += p1[j].z;
+                            v[4 * j + 3] += p1[j].w;
+                        }
+                    }
+                }
+            }
+            finish_chunk(u, c, v, last);
+        }
+    }
+    // drain: C slabs still in flight, then every store
+    if (lane == 0) {
+        for (uint32_t p = gpos; p < ppos; ++p) wait_bar_drain(&cbar[p % ncb], (p / ncb) & 1u, g);
+        bulk_wait_group_all();
+    }
+    __syncwarp();
+}
+
+template <int BN>
+__device__ __forceinline__ void epilogue(const GemmKernelParams& P, const CUtensorMap* tmC, const CUtensorMap* tmD,
+                                         uint32_t tmem_base, uint64_t* tfull, uint64_t* tempty, uint8_t* esmem,
+                                         uint64_t* cbar, volatile uint32_t* bcast, const Guard& g) {
+    if constexpr (BN >= 32) {
+        if (P.epi.tma) {
+            epilogue_tma<BN>(P, tmC, tmD, tmem_base, tfull, tempty, esmem, cbar, bcast, g);
+            return;
+        }
+    }
+    epilogue_role<BN>(P, tmem_base, tfull, tempty, reinterpret_cast<float*>(esmem), bcast, g);
 }
 
 }  // namespace qg

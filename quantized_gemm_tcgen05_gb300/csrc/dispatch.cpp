@@ -133,8 +133,10 @@ std::vector<Choice> candidates(const Problem& p, int sm_count) {
             out.push_back(c);
         }
         if (T < sm_count) {
-            for (int32_t S : {2, 4, 8}) {
-                if (k_iters < 2 * S) break;
+            const int32_t one_wave = (int32_t)(sm_count / T);
+            const bool extra = one_wave != 2 && one_wave != 4 && one_wave != 8;
+            for (int32_t S : {2, 4, 8, extra ? one_wave : 0}) {
+                if (S < 2 || S > 16 || k_iters < 2 * S) continue;
                 c.sched = SCHED_SPLITK;
                 c.splits = S;
                 out.push_back(c);
@@ -154,22 +156,30 @@ std::vector<Choice> candidates(const Problem& p, int sm_count) {
 }
 
 Choice heuristic(const Problem& p, int sm_count) {
+    // Measured on GB300 (152 SMs): full-width 128 x 256 tiles win whenever
+    // there are at least as many tiles as SMs; below that, K is split so all
+    // SMs stream -- into as many equal slices as fill one wave (split-K),
+    // else by stream-K.
     Choice c;
     if (swap_allowed(p) && p.M <= 64) {
         c.swap = 1;
         c.bn = swap_bn(p.M);
     } else {
         c.bn = p.N > 128 ? 256 : 128;
-        if (p.family == FAM_DQ) c.bn = 128;
     }
     c.sched = SCHED_DP;
     if (p.family == FAM_GROUPED) return c;
     SchedParams s = make_sched(p, c, sm_count);
     const int64_t T = total_tiles(s);
     const int64_t k_iters = s.k_iters;
-    const double waves = (double)T / sm_count;
-    const double eff = waves / ceil(waves);
-    if (k_iters >= 4 && eff < 0.9) c.sched = SCHED_STREAMK;
+    if (T >= sm_count || k_iters < 4) return c;
+    const int64_t S = sm_count / T;
+    if (S >= 2) {
+        c.sched = SCHED_SPLITK;
+        c.splits = (int32_t)(S > 8 ? 8 : S);
+    } else {
+        c.sched = SCHED_STREAMK;
+    }
     return c;
 }
 

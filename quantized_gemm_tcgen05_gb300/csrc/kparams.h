@@ -36,19 +36,21 @@ struct EpiParams {
     int32_t d_type;    // DT_F32 / DT_F16 / DT_BF16 (C has the same type)
     int32_t swap;      // 0: tile rows are D rows; 1: tile rows are D columns
     int32_t vec_ok;    // C/D bases and ld allow 16-byte vector access
+    int32_t tma;       // C/D move through shared memory with TMA (tmC / tmD)
+    int32_t ncb;       // shared-memory C/D buffers per epilogue warp (TMA path)
 };
 
 // Group-wise scaling / int4 dequantisation of one shared-memory operand
 // before the tensor core reads it (the role of the scale operands U/V that
 // advance at K-group boundaries).  The operand's value at (row r, k) becomes
 // RN(x[r][k] * scale[k / group][r]) in the MMA input type, with x the int4
-// nibble or the stored 16-bit value.
+// nibble or the stored 16-bit value.  The scale rows a K-step needs are
+// copied into the stage by TMA together with the operand tiles.
 struct OperandXform {
-    const void* scale;   // [K/group][rows], rows contiguous, or NULL (no scaling)
-    int64_t scale_ld;    // elements
-    int64_t rows;        // valid rows of the operand (scale reads are bounded by it)
+    int32_t has_scale;   // scale rows arrive with every stage (TMA), else unscaled
     int32_t scale_type;  // DT_F16 / DT_BF16
-    int32_t group;       // group size along K (multiple of 8)
+    int32_t group;       // group size along K: a multiple of 64, or a divisor of 64 (>= 8)
+    int32_t sc_rows;     // scale rows per 64-wide K-step: max(1, 64 / group)
     int32_t int4;        // operand is packed int4 (raw tile rows of 32 bytes)
     int32_t active;      // any transform at all
 };
@@ -81,10 +83,16 @@ QG_HD uint32_t make_idesc_f16(int ab_is_bf16, int m, int n) {
 }
 
 // Entry points implemented in the .cu files.
-cudaError_t launch_umma_gemm(int bn, const CUtensorMap& tx, const CUtensorMap& ty, const GemmKernelParams& p,
-                             int grid, cudaStream_t st);
-cudaError_t launch_umma_dq_gemm(int bn, const CUtensorMap& tx, const CUtensorMap& ty, const GemmKernelParams& p,
-                                int grid, cudaStream_t st);
+// The four tensor maps of one launch: X and Y operands, C and D (the last two
+// are used only when EpiParams::tma is set).
+struct GemmMaps {
+    CUtensorMap x, y, c, d;
+    CUtensorMap xs, ys;  // scale rows of X / Y (transforming kernel only)
+};
+
+cudaError_t launch_umma_gemm(int bn, const GemmMaps& maps, const GemmKernelParams& p, int grid, cudaStream_t st);
+cudaError_t launch_umma_dq_gemm(int bn, const GemmMaps& maps, const GemmKernelParams& p, int grid,
+                                cudaStream_t st);
 cudaError_t launch_scale_c(const EpiParams& e, int64_t batches, cudaStream_t st);
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t timeout_ns, cudaStream_t st);
 int umma_max_stages(int bn);

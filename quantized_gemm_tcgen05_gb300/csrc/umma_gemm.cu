@@ -34,9 +34,9 @@ struct UmmaCfg {
     static constexpr uint32_t B_BYTES = BN * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
-    static constexpr uint32_t STAGING_BYTES = 4 * 32 * Chunk<BN>::W * 4;
+    static constexpr uint32_t STAGING_BYTES = EPI_SMEM_BYTES;
     static constexpr int MAX_STAGES = 16;
-    static constexpr uint32_t AUX_BYTES = (2 * MAX_STAGES + 5) * 8 + 16;
+    static constexpr uint32_t AUX_BYTES = (2 * MAX_STAGES + 5 + EPI_CBARS) * 8 + 16;
     static constexpr uint32_t FIXED_BYTES = 1024 /*alignment slack*/ + STAGING_BYTES + AUX_BYTES;
     static size_t smem_bytes(int stages) { return FIXED_BYTES + (size_t)stages * STAGE_BYTES; }
     static int max_stages() {
@@ -49,6 +49,7 @@ struct UmmaCfg {
 template <int BN>
 __global__ void __launch_bounds__(192, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
+                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                      const __grid_constant__ GemmKernelParams P) {
     using Cfg = UmmaCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
@@ -61,7 +62,8 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t* tfull = empty + Cfg::MAX_STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* done = tempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    uint64_t* cbar = done + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cbar + EPI_CBARS);
     volatile uint32_t* bcast = tmem_slot + 1;
     volatile uint32_t* abort_flag = tmem_slot + 2;
 
@@ -76,6 +78,7 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(&tempty[b], 128);
         }
         mbar_init(done, 1);
+        for (int i = 0; i < EPI_CBARS; ++i) mbar_init(&cbar[i], 1);
         *bcast = 0;
         *abort_flag = 0;
         fence_barrier_init();
@@ -176,7 +179,7 @@ __global__ void __launch_bounds__(192, 1)
             }
         }
     } else {
-        epilogue_role<BN>(P, tmem_base, tfull, tempty, staging, bcast, g);
+        epilogue<BN>(P, &tmC, &tmD, tmem_base, tfull, tempty, reinterpret_cast<uint8_t*>(staging), cbar, bcast, g);
     }
 
     tc_fence_before_sync();
@@ -219,24 +222,22 @@ __global__ void wait_selftest_kernel(uint32_t* status, uint64_t timeout_ns) {
 }
 
 template <int BN>
-static cudaError_t launch_bn(const CUtensorMap& tx, const CUtensorMap& ty, const GemmKernelParams& p, int grid,
-                             cudaStream_t st) {
+static cudaError_t launch_bn(const GemmMaps& m, const GemmKernelParams& p, int grid, cudaStream_t st) {
     const size_t smem = UmmaCfg<BN>::smem_bytes(p.stages);
     cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    umma_gemm_kernel<BN><<<grid, 192, smem, st>>>(tx, ty, p);
+    umma_gemm_kernel<BN><<<grid, 192, smem, st>>>(m.x, m.y, m.c, m.d, p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_umma_gemm(int bn, const CUtensorMap& tx, const CUtensorMap& ty, const GemmKernelParams& p,
-                             int grid, cudaStream_t st) {
+cudaError_t launch_umma_gemm(int bn, const GemmMaps& m, const GemmKernelParams& p, int grid, cudaStream_t st) {
     switch (bn) {
-        case 16: return launch_bn<16>(tx, ty, p, grid, st);
-        case 32: return launch_bn<32>(tx, ty, p, grid, st);
-        case 64: return launch_bn<64>(tx, ty, p, grid, st);
-        case 128: return launch_bn<128>(tx, ty, p, grid, st);
-        case 256: return launch_bn<256>(tx, ty, p, grid, st);
+        case 16: return launch_bn<16>(m, p, grid, st);
+        case 32: return launch_bn<32>(m, p, grid, st);
+        case 64: return launch_bn<64>(m, p, grid, st);
+        case 128: return launch_bn<128>(m, p, grid, st);
+        case 256: return launch_bn<256>(m, p, grid, st);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -32,6 +32,16 @@ def dev_bits(bits, dtype):
     return t.view(TORCH_DT[dtype]).cuda()
 
 
+def padded_rows(bits, dtype):
+    """A 2-D scale matrix on the device with its row stride rounded up to 8
+    elements; returns (tensor, ld)."""
+    rows, cols = bits.shape
+    ld = -(-cols // 8) * 8
+    t = torch.zeros(rows, ld, dtype=TORCH_DT[dtype], device="cuda")
+    t[:, :cols] = dev_bits(bits, dtype)
+    return t, ld
+
+
 def tolerance(ref, bound, d_type):
     tol = 1e-5 * bound + 1e-6
     if d_type != synth.F32:
@@ -82,12 +92,12 @@ def run_problem(lib, p, o=None, D=None, C=None, stream=None, workspace=True):
     if C is not None:
         Cd = qg.row_major(C)
     U = Ud = V = Vd = None
-    if p.U is not None:
-        U = dev_bits(p.U, p.u_type)
-        Ud = qg.layout(p.u_type, qg.GEMM_ROW_MAJOR, p.K // p.ga, p.M, p.M)
+    if p.U is not None:  # scale rows padded to a multiple of 8 elements (16 bytes)
+        U, ldu = padded_rows(p.U, p.u_type)
+        Ud = qg.layout(p.u_type, qg.GEMM_ROW_MAJOR, p.K // p.ga, p.M, ldu)
     if p.V is not None:
-        V = dev_bits(p.V, p.v_type)
-        Vd = qg.layout(p.v_type, qg.GEMM_ROW_MAJOR, p.K // p.gb, p.N, p.N)
+        V, ldv = padded_rows(p.V, p.v_type)
+        Vd = qg.layout(p.v_type, qg.GEMM_ROW_MAJOR, p.K // p.gb, p.N, ldv)
     st = stream if stream is not None else qg.current_stream()
     rc = qg.gemm_run(lib.h, o, p.alpha, qg.ptr(A), Ad, qg.ptr(U), Ud, qg.ptr(B), Bd, qg.ptr(V), Vd, p.beta,
                      qg.ptr(C), Cd, qg.ptr(D), Dd, lib.ws.c if workspace else None, st)

@@ -124,3 +124,26 @@ def test_int4_without_scales(lib):
     assert rc == 0
     ref, bound = oracle.gemm(p)
     assert_close(D.double().cpu().numpy(), ref, bound, p.d_type, "int4 no V")
+
+
+def test_scale_layout_rules(lib):
+    import quantized_gemm_tcgen05_gb300 as qg
+    import torch
+    M, N, K = 64, 128, 256
+    A = torch.zeros(M, K, dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros(N, K, dtype=torch.bfloat16, device="cuda")
+    D = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+    V = torch.ones(K // 64, N + 8, dtype=torch.bfloat16, device="cuda")
+
+    def call(gb, ldv, vptr=None):
+        Vd = qg.layout(qg.GEMM_BF16, qg.GEMM_ROW_MAJOR, K // gb, N, ldv)
+        return qg.gemm_run(lib.h, op(gb=gb), 1.0, qg.ptr(A), qg.row_major(A), None, None, qg.ptr(B),
+                           qg.col_major_from_nk(B), vptr or qg.ptr(V), Vd, 0.0, None, None, qg.ptr(D),
+                           qg.row_major(D), lib.ws.c, qg.current_stream())
+
+    assert call(64, N + 8) == 0
+    assert call(64, N + 3) == qg.GEMM_ERR_INVALID_ARG         # ld not a multiple of 16 bytes
+    assert call(64, N + 8, qg.ptr(V) + 2) == qg.GEMM_ERR_INVALID_ARG
+    assert call(48, N + 8) == qg.GEMM_ERR_INVALID_ARG          # neither divides nor is a multiple of 64
+    assert call(0, N + 8) == qg.GEMM_ERR_INVALID_ARG           # V given without a group size
+    torch.cuda.synchronize()
