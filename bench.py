@@ -233,16 +233,17 @@ class Runner:
                  Vd=qg.layout(p.v_type, qg.GEMM_ROW_MAJOR, p.K // p.gb, p.N, p.N) if V is not None else None)
         return d
 
-    def run(self, s):
+    def run(self, s, stream=None):
         qg, p, a = self.qg, self.p, self.args[s]
+        st = stream if stream is not None else self.stream
         if self.grouped:
             rc = qg.gemm_run_grouped(self.h, self.op, p.alpha, a["A"].data_ptr(), a["Ad"], None, None,
                                      a["B"].data_ptr(), a["Bd"], None, None, p.beta, None, None, a["D"].data_ptr(),
-                                     a["Dd"], a["off"].data_ptr(), len(p.counts), self.ws.c, self.stream)
+                                     a["Dd"], a["off"].data_ptr(), len(p.counts), self.ws.c, st)
         else:
             rc = qg.gemm_run(self.h, self.op, p.alpha, a["A"].data_ptr(), a["Ad"], None, None, a["B"].data_ptr(),
                              a["Bd"], qg.ptr(a["V"]), a["Vd"], p.beta, qg.ptr(a["C"]), a["Cd"], a["D"].data_ptr(),
-                             a["Dd"], self.ws.c, self.stream)
+                             a["Dd"], self.ws.c, st)
         if rc:
             raise RuntimeError(f"gemm_run failed: {qg.gemm_status_string(rc)}")
 
@@ -283,24 +284,50 @@ def run_ours(args, rank, world, cfg):
         raise RuntimeError("device status reported a timeout during warm-up")
     choice = qg.gemm_last_choice(R.h)
 
-    # timed region: K steps, events around every launch on the launching stream
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
-    t0 = time.time()
-    start.record(stream)
-    for i in range(args.steps):
-        evs[i][0].record(stream)
-        R.run(i % sets)
-        evs[i][1].record(stream)
-    end.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    t1 = time.time()
+    # timed region: K steps.  Eager: one gemm_run per step with CUDA events
+    # around every launch on the launching stream.  Graph: the K gemm_run
+    # calls captured once into a CUDA graph (as an engine replaying its layers
+    # would), replayed once untimed, then timed as one replay.
+    launch_ms = None
+    if args.launch == "graph":
+        cap = torch.cuda.Stream()
+        graph = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(args.steps):
+                R.run(i % sets, qg.current_stream())
+        graph.replay()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        start.record(stream)
+        graph.replay()
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        t1 = time.time()
+        total_ms = start.elapsed_time(end)
+    else:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        start.record(stream)
+        for i in range(args.steps):
+            evs[i][0].record(stream)
+            R.run(i % sets)
+            evs[i][1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        t1 = time.time()
+        total_ms = start.elapsed_time(end)
+        launch_ms = [a.elapsed_time(b) for a, b in evs]
     sampler.stop()
-    total_ms = start.elapsed_time(end)
-    launch_ms = [a.elapsed_time(b) for a, b in evs]
     if dist is not None:
         t = torch.tensor([total_ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -317,7 +344,10 @@ def run_ours(args, rank, world, cfg):
         e2e = measure_e2e(R, torch, unit_per_step, unit, world, dist, steps=max(3, min(20, args.steps)))
 
     peaks, peak_src = load_peaks()
-    avg_launch_s = statistics.mean(launch_ms) / 1e3
+    # per-launch duration: the event pair around each launch (eager), or the
+    # graph replay divided by its launches (back-to-back kernels, so this also
+    # charges the inter-kernel gaps to the kernel: a conservative figure)
+    avg_launch_s = (statistics.mean(launch_ms) if launch_ms else ms_per_step) / 1e3
     if bound == "hbm":
         achieved = abytes / avg_launch_s / 1e9
         peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -334,6 +364,7 @@ def run_ours(args, rank, world, cfg):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if p.a_type == synth.BF16 else "f16",
         "data": "synthetic (seeded, shapes and distributions of the workload)",
         "config": {"workload": WORKLOADS[cfg]["desc"], "kernel": choice, "parallelism": f"replicas x{world}",
+                   "launch": "CUDA graph of the K gemm_run calls" if args.launch == "graph" else "eager gemm_run per step",
                    "l2": f"{sets} rotating input sets ({sets * one_set / 1e6:.0f} MB) so operands are not L2-resident"},
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": r_unit,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -483,6 +514,7 @@ def main():
     ap.add_argument("--config", choices=sorted(WORKLOADS), default="c2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--launch", choices=["graph", "eager"], default="graph")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -34,6 +34,17 @@ struct gemm_handle {
     bool log = false;
     int force_splitk = 0;
     uint64_t timeout_ns = 2000000000ull;
+    // Host-path caches: tensor maps by their encode arguments (direct-mapped)
+    // and recently validated device pointers (ring).  They keep a repeated
+    // gemm_run call to a few microseconds of host work.
+    struct MapEntry {
+        uint64_t key[16];
+        CUtensorMap map;
+        bool valid;
+    };
+    MapEntry maps[128] = {};
+    const void* dev_ptrs[64] = {};
+    int dev_ptr_next = 0;
 };
 
 namespace {
@@ -42,7 +53,7 @@ bool is16(int32_t t) { return t == GEMM_F16 || t == GEMM_BF16; }
 bool is_float_out(int32_t t) { return t == GEMM_F32 || t == GEMM_F16 || t == GEMM_BF16; }
 int64_t elem_bytes_x2(int32_t t) { return t == GEMM_F32 ? 8 : (t == GEMM_S4 ? 1 : 4); }  // 2 * bytes
 
-bool device_pointer(const void* p) {
+bool device_pointer_uncached(const void* p) {
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
         cudaGetLastError();
@@ -52,6 +63,45 @@ bool device_pointer(const void* p) {
 }
 
 // Validate one operand layout against the expected shape and order.
+bool device_pointer(gemm_handle* h, const void* p) {
+    for (const void* q : h->dev_ptrs)
+        if (q == p) return true;
+    if (!device_pointer_uncached(p)) return false;
+    h->dev_ptrs[h->dev_ptr_next] = p;
+    h->dev_ptr_next = (h->dev_ptr_next + 1) % 64;
+    return true;
+}
+
+// cuTensorMapEncodeTiled through the handle's cache (same arguments, same map).
+CUresult encode_cached(gemm_handle* h, CUtensorMap* m, CUtensorMapDataType dt, cuuint32_t rank, const void* ptr,
+                       const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                       CUtensorMapSwizzle swz) {
+    uint64_t key[16] = {0};
+    key[0] = (uint64_t)dt | ((uint64_t)rank << 8) | ((uint64_t)swz << 16);
+    key[1] = reinterpret_cast<uintptr_t>(ptr);
+    for (cuuint32_t i = 0; i < rank && i < 5; ++i) {
+        key[2 + i] = dims[i];
+        key[7 + i] = box[i];
+        if (i + 1 < rank) key[12 + i] = strides[i];
+    }
+    uint64_t hsh = 1469598103934665603ull;
+    for (uint64_t k : key) hsh = (hsh ^ k) * 1099511628211ull;
+    gemm_handle::MapEntry& e = h->maps[hsh % 128];
+    if (e.valid && memcmp(e.key, key, sizeof key) == 0) {
+        *m = e.map;
+        return CUDA_SUCCESS;
+    }
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    CUresult r = h->encode(m, dt, rank, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS) {
+        memcpy(e.key, key, sizeof key);
+        e.map = *m;
+        e.valid = true;
+    }
+    return r;
+}
+
 int check_layout(const gemm_layout_t* d, int32_t order, int64_t rows, int64_t cols) {
     if (!d) return GEMM_ERR_INVALID_ARG;
     if (d->order != order) return GEMM_ERR_UNSUPPORTED;
@@ -143,11 +193,8 @@ int make_map(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t type, int6
     cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)batches};
     cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)bstride * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-    cuuint32_t es[3] = {1, 1, 1};
     const cuuint32_t rank = batches > 1 ? 3 : 2;
-    CUresult r = h->encode(m, dt, rank, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode_cached(h, m, dt, rank, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -159,10 +206,8 @@ int make_map_s4(gemm_handle* h, CUtensorMap* m, const void* ptr, int64_t K, int6
     cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(ld_nibbles / 2)};
     cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
-    cuuint32_t es[2] = {1, 1};
-    CUresult r = h->encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode_cached(h, m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -178,11 +223,9 @@ int make_map_cd(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t type, i
     cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)batches};
     cuuint64_t strides[2] = {(cuuint64_t)(ld * es), (cuuint64_t)(bstride * es)};
     cuuint32_t box[3] = {32, 32, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
     const cuuint32_t rank = batches > 1 ? 3 : 2;
-    CUresult r = h->encode(m, dt, rank, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           es == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode_cached(h, m, dt, rank, ptr, dims, strides, box,
+                               es == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -193,11 +236,8 @@ int make_map_scale(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t type
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)groups};
     cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
     cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
     CUtensorMapDataType dt = type == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUresult r = h->encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = encode_cached(h, m, dt, 2, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -573,10 +613,10 @@ int build_problem(gemm_handle* h, const gemm_op_t* op, float alpha, const void* 
         } else if ((p.ldb * 2) % 16 || (p.b_bs * 2) % 16) {
             return GEMM_ERR_INVALID_ARG;
         }
-        if (!device_pointer(A) || !device_pointer(B)) return GEMM_ERR_INVALID_ARG;
+        if (!device_pointer(h, A) || !device_pointer(h, B)) return GEMM_ERR_INVALID_ARG;
     }
-    if (!device_pointer(D)) return GEMM_ERR_INVALID_ARG;
-    if (p.C && !device_pointer(p.C)) return GEMM_ERR_INVALID_ARG;
+    if (!device_pointer(h, D)) return GEMM_ERR_INVALID_ARG;
+    if (p.C && !device_pointer(h, p.C)) return GEMM_ERR_INVALID_ARG;
     (void)elem_bytes_x2;
     *out = p;
     return GEMM_OK;
@@ -627,7 +667,7 @@ int gemm_run_grouped(gemm_handle_t h, const gemm_op_t* op, float alpha, const vo
     Problem p;
     rc = build_problem(h, op, alpha, A, Adesc, U, Udesc, B, Bdesc, V, Vdesc, beta, C, Cdesc, D, Ddesc, true, &p);
     if (rc) return rc;
-    if (!device_pointer(expert_offsets_dev) || (reinterpret_cast<uintptr_t>(expert_offsets_dev) & 3u))
+    if (!device_pointer(h, expert_offsets_dev) || (reinterpret_cast<uintptr_t>(expert_offsets_dev) & 3u))
         return GEMM_ERR_INVALID_ARG;
     p.offsets = expert_offsets_dev;
     p.num_experts = num_experts;

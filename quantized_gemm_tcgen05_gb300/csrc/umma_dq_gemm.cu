@@ -18,6 +18,8 @@
 // The product of a nibble or a 16-bit value with an fp16/bf16 scale is exact
 // in fp32, so each operand element is rounded exactly once, to the MMA input
 // type (A's type).
+#include <atomic>
+
 #include "common.cuh"
 
 namespace qg {
@@ -352,9 +354,18 @@ __global__ void __launch_bounds__(320, 1)
 template <int BN>
 static cudaError_t launch_dq_bn(const GemmMaps& m, const GemmKernelParams& p, int grid, cudaStream_t st) {
     const size_t smem = DqCfg<BN>::smem_bytes(p.stages);
-    cudaError_t e = cudaFuncSetAttribute(umma_dq_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    // raise the dynamic shared-memory limit once per device (to the largest ring)
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load() & bit)) {
+        e = cudaFuncSetAttribute(umma_dq_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)DqCfg<BN>::smem_bytes(DqCfg<BN>::max_stages()));
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit);
+    }
     umma_dq_gemm_kernel<BN><<<grid, 320, smem, st>>>(m.x, m.y, m.c, m.d, m.xs, m.ys, p);
     return cudaGetLastError();
 }

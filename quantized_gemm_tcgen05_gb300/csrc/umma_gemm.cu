@@ -22,6 +22,8 @@
 // need no special code: TMA fills out-of-range elements with zeros (the
 // zero-fill rule of the DeepGEMM kernel-set blog, section 4.3) and the
 // epilogue masks the stores.
+#include <atomic>
+
 #include "common.cuh"
 
 namespace qg {
@@ -224,9 +226,18 @@ __global__ void wait_selftest_kernel(uint32_t* status, uint64_t timeout_ns) {
 template <int BN>
 static cudaError_t launch_bn(const GemmMaps& m, const GemmKernelParams& p, int grid, cudaStream_t st) {
     const size_t smem = UmmaCfg<BN>::smem_bytes(p.stages);
-    cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    // raise the dynamic shared-memory limit once per device (to the largest ring)
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load() & bit)) {
+        e = cudaFuncSetAttribute(umma_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)UmmaCfg<BN>::smem_bytes(UmmaCfg<BN>::max_stages()));
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit);
+    }
     umma_gemm_kernel<BN><<<grid, 192, smem, st>>>(m.x, m.y, m.c, m.d, p);
     return cudaGetLastError();
 }

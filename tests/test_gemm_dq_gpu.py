@@ -136,7 +136,7 @@ def test_scale_layout_rules(lib):
     V = torch.ones(K // 64, N + 8, dtype=torch.bfloat16, device="cuda")
 
     def call(gb, ldv, vptr=None):
-        Vd = qg.layout(qg.GEMM_BF16, qg.GEMM_ROW_MAJOR, K // gb, N, ldv)
+        Vd = qg.layout(qg.GEMM_BF16, qg.GEMM_ROW_MAJOR, K // (gb or 64), N, ldv)
         return qg.gemm_run(lib.h, op(gb=gb), 1.0, qg.ptr(A), qg.row_major(A), None, None, qg.ptr(B),
                            qg.col_major_from_nk(B), vptr or qg.ptr(V), Vd, 0.0, None, None, qg.ptr(D),
                            qg.row_major(D), lib.ws.c, qg.current_stream())
