@@ -156,6 +156,37 @@ int gemm_run(gemm_handle_t h, const gemm_op_t* op, float alpha,
              const gemm_workspace_t* workspace, gemm_stream_t stream);
 
 /*
+ * gemm_run without a workspace argument, for callers that cannot allocate
+ * device memory (for example code running under a stream capture that forbids
+ * allocation, or inside a host whose allocator hands out no scratch).  The
+ * pages have no counterpart to this entry point.
+ *   - Scratch for split-K / stream-K comes from a fixed array in the library's
+ *     own device memory: 64 KB of tile counters and 8 MB of fp32 partials
+ *     (GEMM_NOALLOC_BARRIERS_SIZE / GEMM_NOALLOC_PARTIALS_SIZE).  Every GPU
+ *     that loads the library holds it until the process exits.
+ *   - A problem whose chosen or forced schedule needs more scratch than that is
+ *     rejected with GEMM_ERR_WORKSPACE (automatic choices fall back to an
+ *     unsplit schedule instead).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Each call clears the counters on `stream` (cudaMemsetAsync) and then
+ *     behaves as gemm_run.  It calls no cudaMalloc / cudaFree.
+ *   - All calls share the one array: calls that may overlap on the GPU (other
+ *     streams, other threads) race and must be serialised by the caller.
+ */
+#define GEMM_NOALLOC_BARRIERS_SIZE ((size_t)64 << 10)
+#define GEMM_NOALLOC_PARTIALS_SIZE ((size_t)8 << 20)
+int gemm_run_noalloc(gemm_handle_t h, const gemm_op_t* op, float alpha,
+                     const void* A, const gemm_layout_t* Adesc,
+                     const void* U, const gemm_layout_t* Udesc,
+                     const void* B, const gemm_layout_t* Bdesc,
+                     const void* V, const gemm_layout_t* Vdesc,
+                     float beta,
+                     const void* C, const gemm_layout_t* Cdesc,
+                     void* D, const gemm_layout_t* Ddesc,
+                     gemm_stream_t stream);
+
+/*
  * Grouped (MoE) GEMM, after the grouped GEMM of the TileLang tutorial
  * "gemm_variants.py" (section gemm_grouped): the rows of A are sorted by
  * expert, expert e owning rows expert_offsets[e] .. expert_offsets[e+1]-1, and

@@ -31,12 +31,15 @@ GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
 GEMM_DISPATCH_DEFAULT, GEMM_DISPATCH_MEASURE, GEMM_DISPATCH_REUSE = 0, 1, 2
 GEMM_BARRIERS_SIZE = 1 << 20
 GEMM_PARTIALS_SIZE = 32 << 20
+GEMM_NOALLOC_BARRIERS_SIZE = 64 << 10
+GEMM_NOALLOC_PARTIALS_SIZE = 8 << 20
 
 # Every exported symbol of gemm.h.
 SYMBOLS = (
     "gemm_create", "gemm_destroy", "gemm_run", "gemm_run_grouped", "gemm_export", "gemm_import",
     "gemm_get_tuning_seq", "gemm_cache_size", "gemm_status_string", "gemm_device_status",
     "gemm_selftest_wait_timeout", "gemm_last_choice", "gemm_plan_streamk", "gemm_grouped_block",
+    "gemm_run_noalloc",
 )
 
 
@@ -85,6 +88,8 @@ def lib():
         "gemm_destroy": (ctypes.c_int, [P]),
         "gemm_run": (ctypes.c_int, [P, ctypes.POINTER(gemm_op_t), F, P, LP, P, LP, P, LP, P, LP, F, P, LP, P, LP,
                                     ctypes.POINTER(gemm_workspace_t), P]),
+        "gemm_run_noalloc": (ctypes.c_int, [P, ctypes.POINTER(gemm_op_t), F, P, LP, P, LP, P, LP, P, LP, F, P, LP, P,
+                                            LP, P]),
         "gemm_run_grouped": (ctypes.c_int, [P, ctypes.POINTER(gemm_op_t), F, P, LP, P, LP, P, LP, P, LP, F, P, LP,
                                             P, LP, P, I32, ctypes.POINTER(gemm_workspace_t), P]),
         "gemm_export": (ctypes.c_int, [P, P, SZ, ctypes.POINTER(SZ)]),
@@ -134,6 +139,13 @@ def gemm_run(h, op, alpha, A, Adesc, U, Udesc, B, Bdesc, V, Vdesc, beta, C, Cdes
     """Returns the status code (0 = OK).  Pointers are ints (device addresses)."""
     return lib().gemm_run(h, ctypes.byref(op), float(alpha), A, _lp(Adesc), U, _lp(Udesc), B, _lp(Bdesc), V,
                           _lp(Vdesc), float(beta), C, _lp(Cdesc), D, _lp(Ddesc), _lp(workspace), stream)
+
+
+def gemm_run_noalloc(h, op, alpha, A, Adesc, U, Udesc, B, Bdesc, V, Vdesc, beta, C, Cdesc, D, Ddesc, stream):
+    """gemm_run whose split-K / stream-K scratch is the library's own fixed
+    device array (no workspace argument, no allocation)."""
+    return lib().gemm_run_noalloc(h, ctypes.byref(op), float(alpha), A, _lp(Adesc), U, _lp(Udesc), B, _lp(Bdesc), V,
+                                  _lp(Vdesc), float(beta), C, _lp(Cdesc), D, _lp(Ddesc), stream)
 
 
 def gemm_run_grouped(h, op, alpha, A, Adesc, U, Udesc, B, Bdesc, V, Vdesc, beta, C, Cdesc, D, Ddesc,

@@ -18,6 +18,7 @@
 #include <vector>
 
 #include "dispatch.h"
+#include "handle_internal.h"
 #include "kparams.h"
 
 using namespace qg;
@@ -115,6 +116,8 @@ int check_layout(const gemm_layout_t* d, int32_t order, int64_t rows, int64_t co
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+int qg::handle_device(gemm_handle_t h) { return h ? h->device : -1; }
 
 extern "C" {
 
