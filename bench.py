@@ -119,9 +119,11 @@ def kernel_source_hash():
 def profile_traffic(cfg):
     """Per-launch DRAM bytes from the committed ncu summary of this workload,
     or None when it is missing or was taken on other kernel sources."""
-    path = os.path.join(ROOT, "profiles", f"umma_gemm_{cfg}.md")
-    if not os.path.exists(path):
+    import glob
+    found = sorted(glob.glob(os.path.join(ROOT, "profiles", f"*_{cfg}.md")))
+    if not found:
         return None
+    path = found[0]
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     s = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
@@ -452,20 +454,21 @@ def oracle_sample(p, rows):
     return q
 
 
-def cpu_baseline(p, cfg, unit, target_s=12.0):
+def cpu_baseline(p, cfg, unit, target_s=10.0):
+    """The oracle on the first rows of the workload, doubling the row count
+    until one call takes about target_s (or the whole problem is covered)."""
     import oracle
 
+    full_rows = int(p.counts.max()) if hasattr(p, "counts") else p.M
     rows = 8
-    q = oracle_sample(p, rows)
-    t = time.perf_counter()
-    oracle.gemm(q)
-    dt = time.perf_counter() - t
-    if dt < target_s / 4 and q.M < (p.M if not hasattr(p, "counts") else int(p.counts.max())):
-        rows = int(min(4096, max(8, rows * target_s / 2 / max(dt, 1e-3))))
+    while True:
         q = oracle_sample(p, rows)
         t = time.perf_counter()
         oracle.gemm(q)
         dt = time.perf_counter() - t
+        if dt >= target_s or q.M >= full_rows or rows >= 4096:
+            break
+        rows = min(full_rows, rows * 2 if dt > target_s / 8 else rows * 4)
     f = flops_of(q)
     val = (algorithmic_bytes(q) / dt / 1e9) if unit == "GB/s" else f / dt / 1e12
     return {"value": round(val, 6), "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",

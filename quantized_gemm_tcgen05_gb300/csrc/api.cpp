@@ -422,7 +422,9 @@ bool forced_kernel(const Problem& p, Choice* out) {
     } else {
         return false;
     }
-    if (!(c.bn == 16 || c.bn == 32 || c.bn == 64 || c.bn == 128 || c.bn == 256)) return false;
+    if (!(c.bn == 16 || c.bn == 32 || c.bn == 64 || c.bn == 128 || c.bn == 192 || c.bn == 224 || c.bn == 256))
+        return false;
+    if (p.family == FAM_DQ && (c.bn == 192 || c.bn == 224)) return false;
     if (c.swap && (p.family == FAM_GROUPED || p.batches != 1)) return false;
     if (p.family == FAM_GROUPED) c.sched = SCHED_DP;
     *out = c;

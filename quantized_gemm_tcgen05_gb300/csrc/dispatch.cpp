@@ -150,7 +150,8 @@ std::vector<Choice> candidates(const Problem& p, int sm_count) {
         return out;
     }
     add_scheds(128, 0);
-    if (p.N > 128) add_scheds(256, 0);
+    if (p.N > 128)
+        for (int32_t bn : {192, 224, 256}) add_scheds(bn, 0);
     if (swap_allowed(p)) add_scheds(swap_bn(p.M), 1);
     return out;
 }
@@ -164,8 +165,24 @@ Choice heuristic(const Problem& p, int sm_count) {
     if (swap_allowed(p) && p.M <= 64) {
         c.swap = 1;
         c.bn = swap_bn(p.M);
+    } else if (p.family == FAM_DQ || p.N <= 128) {
+        c.bn = 128;
+    } else if (p.family == FAM_GROUPED) {
+        c.bn = 256;  // measured best for ragged MoE blocks (the tile count is only an upper bound)
     } else {
-        c.bn = p.N > 128 ? 256 : 128;
+        // the tile width that minimises waves x width (time per wave grows
+        // with the width); wider wins ties
+        int64_t best = -1;
+        for (int32_t bn : {256, 224, 192, 128}) {
+            Choice t;
+            t.bn = bn;
+            const int64_t T = total_tiles(make_sched(p, t, sm_count));
+            const int64_t cost = ceil_div(T, sm_count) * bn;
+            if (best < 0 || cost < best) {
+                best = cost;
+                c.bn = bn;
+            }
+        }
     }
     c.sched = SCHED_DP;
     if (p.family == FAM_GROUPED) return c;
@@ -230,7 +247,7 @@ std::string cache_serialize(const std::map<Key, Choice>& cache, const std::strin
 }
 
 static bool valid_choice(const Key& k, const Choice& c) {
-    const bool bn_ok = c.bn == 16 || c.bn == 32 || c.bn == 64 || c.bn == 128 || c.bn == 256;
+    const bool bn_ok = c.bn == 16 || c.bn == 32 || c.bn == 64 || c.bn == 128 || c.bn == 192 || c.bn == 224 || c.bn == 256;
     if (!bn_ok || (c.swap != 0 && c.swap != 1) || c.sched < SCHED_DP || c.sched > SCHED_STREAMK) return false;
     if (c.splits < 1 || c.splits > 64 || !(c.us >= 0.0f)) return false;
     if (k.family < FAM_DENSE || k.family > FAM_GROUPED) return false;

@@ -82,6 +82,10 @@ QG_HD uint32_t make_idesc_f16(int ab_is_bf16, int m, int n) {
     return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
+// Tile widths (UMMA N) instantiated for each kernel.
+#define QG_FOR_EACH_DENSE_BN(X) X(16) X(32) X(64) X(128) X(192) X(224) X(256)
+#define QG_FOR_EACH_DQ_BN(X) X(16) X(32) X(64) X(128) X(256)
+
 // Entry points implemented in the .cu files.
 // The four tensor maps of one launch: X and Y operands, C and D (the last two
 // are used only when EpiParams::tma is set).
@@ -89,6 +93,17 @@ struct GemmMaps {
     CUtensorMap x, y, c, d;
     CUtensorMap xs, ys;  // scale rows of X / Y (transforming kernel only)
 };
+
+// Per-width launchers (explicitly instantiated in umma_gemm_bn*.cu and
+// umma_dq_gemm_bn*.cu).
+template <int BN>
+cudaError_t launch_umma_bn(const GemmMaps& m, const GemmKernelParams& p, int grid, cudaStream_t st);
+template <int BN>
+int umma_stages_bn();
+template <int BN>
+cudaError_t launch_dq_bn(const GemmMaps& m, const GemmKernelParams& p, int grid, cudaStream_t st);
+template <int BN>
+int dq_stages_bn();
 
 cudaError_t launch_umma_gemm(int bn, const GemmMaps& maps, const GemmKernelParams& p, int grid, cudaStream_t st);
 cudaError_t launch_umma_dq_gemm(int bn, const GemmMaps& maps, const GemmKernelParams& p, int grid,

@@ -1,0 +1,379 @@
+// tcgen05 GEMM with in-mainloop operand transforms: int4 dequantisation and
+// group-wise scaling (the U/V scale operands that advance at K-group
+// boundaries, "InternLM Lmdeploy Gemm MainloopSm80V2", section Description).
+//
+// Same persistent warp-specialised structure as the dense kernel, plus four
+// transform warps between the TMA ring and the tensor core:
+//
+//   warp 0      TMA: X tile (128 x 64 16-bit, SWIZZLE_128B, or 128 x 32 bytes
+//               of packed int4) and Y tile (BN x 64 16-bit, or BN x 32 bytes
+//               of int4) into stage s, arming full[s].
+//   warp 1      TMEM owner / MMA issuer; waits ready[s], not full[s].
+//   warps 2-5   epilogue (shared with the dense kernel).
+//   warps 6-9   transform: wait full[s]; for every 16-byte chunk of 8 K
+//               values of a transformed operand, form RN(x * scale) in fp32
+//               and write the chunk where the SWIZZLE_128B canonical layout
+//               wants it; fence the writes to the async proxy; arrive ready[s].
+//
+// The product of a nibble or a 16-bit value with an fp16/bf16 scale is exact
+// in fp32, so each operand element is rounded exactly once, to the MMA input
+// type (A's type).
+#pragma once
+#include <atomic>
+
+#include "common.cuh"
+
+namespace qg {
+
+template <int BN>
+struct DqCfg {
+    static constexpr uint32_t X_OP = BM * BK * 2;   // 16 KB
+    static constexpr uint32_t Y_OP = BN * BK * 2;
+    static constexpr uint32_t X_RAW = BM * 32;      // packed int4 rows
+    static constexpr uint32_t Y_RAW = BN * 32;
+    static constexpr uint32_t X_SC = BM * 2 * 8;    // up to 8 scale rows (group 8) of 16-bit scales
+    static constexpr uint32_t Y_SC = BN * 2 * 8;
+    static constexpr uint32_t STAGE_BYTES = ((X_OP + Y_OP + X_RAW + Y_RAW + X_SC + Y_SC) + 1023) / 1024 * 1024;
+    static constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * BN);
+    static constexpr uint32_t STAGING_BYTES = EPI_SMEM_BYTES;
+    static constexpr int MAX_STAGES = 12;
+    static constexpr uint32_t AUX_BYTES = (3 * MAX_STAGES + 5 + EPI_CBARS) * 8 + 16;
+    static constexpr uint32_t FIXED_BYTES = 1024 + STAGING_BYTES + AUX_BYTES;
+    static size_t smem_bytes(int stages) { return FIXED_BYTES + (size_t)stages * STAGE_BYTES; }
+    static int max_stages() {
+        int s = (int)((232448 - FIXED_BYTES) / STAGE_BYTES);
+        return s > MAX_STAGES ? MAX_STAGES : s;
+    }
+};
+
+__device__ __forceinline__ uint32_t pack2(float a, float b, int out_bf16) {
+    if (out_bf16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float2 unpack2(uint32_t w, int is_bf16) {
+    if (is_bf16) return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w));
+    return __half22float2(*reinterpret_cast<__half2*>(&w));
+}
+
+// Chunk i of a transform thread covers 16-byte chunk c = tid + 128*i of a
+// ROWS x 64 tile: row c/8 and logical K-chunk j (8 values at k0 + 8j).  For a
+// packed int4 operand j = c % 8 (the destination is permuted); for a 16-bit
+// operand already in the swizzled layout the physical chunk is c % 8 and the
+// logical one is (c % 8) ^ (row % 8).
+template <int ROWS>
+struct XformChunks {
+    static constexpr int N = ROWS / 16;  // chunks per transform thread
+};
+
+// Scale of row r for logical K-chunk j, from the stage's scale rows
+// ([sc_rows][ROWS] 16-bit values; row t covers K-group k0/group + t).  Branch
+// free so the chunks of a thread interleave.
+template <int ROWS>
+__device__ __forceinline__ float stage_scale(const OperandXform& o, const uint8_t* sc, int r, int j) {
+    const int t = o.group >= 64 ? 0 : (8 * j) / o.group;
+    const uint32_t bits = reinterpret_cast<const uint16_t*>(sc)[t * ROWS + r];
+    const float as_f16 = __half2float(__ushort_as_half((unsigned short)bits));
+    const float as_bf16 = __uint_as_float(bits << 16);
+    const float v = o.scale_type == DT_F16 ? as_f16 : as_bf16;
+    return o.has_scale ? v : 1.0f;
+}
+
+template <bool OUT_BF16>
+__device__ __forceinline__ uint32_t pack2t(float a, float b) {
+    if constexpr (OUT_BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+// Transform one operand tile of ROWS rows.  op: the SWIZZLE_128B operand
+// tile; raw: the packed int4 tile (ROWS x 32 bytes); sc: the scale rows.
+// All chunks of a thread are independent; scales and raw words are read
+// first so their shared-memory latency overlaps.
+template <int ROWS, bool INT4, bool OUT_BF16>
+__device__ __forceinline__ void transform_tile(const OperandXform& o, uint8_t* op, const uint8_t* raw,
+                                               const uint8_t* sc, int tid) {
+    constexpr int NC = XformChunks<ROWS>::N;
+    float s[NC];
+    uint32_t w[NC];
+    uint4 in[NC];
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+        const int c = tid + 128 * i;
+        const int r = c >> 3;
+        const int j = INT4 ? (c & 7) : ((c & 7) ^ (r & 7));
+        s[i] = stage_scale<ROWS>(o, sc, r, j);
+        if constexpr (INT4)
+            w[i] = *reinterpret_cast<const uint32_t*>(raw + r * 32 + 4 * (c & 7));
+        else
+            in[i] = *reinterpret_cast<const uint4*>(op + r * 128 + ((c & 7) << 4));
+    }
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+        const int c = tid + 128 * i;
+        const int r = c >> 3;
+        uint4 out;
+        if constexpr (INT4) {
+            // chunk j = c % 8 holds k = k0 + 8j .. +7 (raw bytes 4j .. 4j+3);
+            // biased nibble b = q + 8 becomes the float 2^23 + b, so q = f - (2^23 + 8)
+            const uint32_t x = w[i] ^ 0x88888888u;
+            const uint32_t lo = x & 0x0F0F0F0Fu, hi = (x >> 4) & 0x0F0F0F0Fu;
+            float q[8];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                q[2 * t] = (__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7650u | t)) - 8388616.0f) * s[i];
+                q[2 * t + 1] = (__uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7650u | t)) - 8388616.0f) * s[i];
+            }
+            out.x = pack2t<OUT_BF16>(q[0], q[1]);
+            out.y = pack2t<OUT_BF16>(q[2], q[3]);
+            out.z = pack2t<OUT_BF16>(q[4], q[5]);
+            out.w = pack2t<OUT_BF16>(q[6], q[7]);
+            *reinterpret_cast<uint4*>(op + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = out;
+        } else {
+            const uint32_t iw[4] = {in[i].x, in[i].y, in[i].z, in[i].w};
+            uint32_t ow[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float2 f = unpack2(iw[t], OUT_BF16);
+                ow[t] = pack2t<OUT_BF16>(f.x * s[i], f.y * s[i]);
+            }
+            *reinterpret_cast<uint4*>(op + r * 128 + ((c & 7) << 4)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        }
+    }
+}
+
+template <int ROWS>
+__device__ __forceinline__ void transform_any(const OperandXform& o, uint8_t* op, const uint8_t* raw,
+                                              const uint8_t* sc, int out_bf16, int tid) {
+    if (o.int4) {
+        if (out_bf16)
+            transform_tile<ROWS, true, true>(o, op, raw, sc, tid);
+        else
+            transform_tile<ROWS, true, false>(o, op, raw, sc, tid);
+    } else {
+        if (out_bf16)
+            transform_tile<ROWS, false, true>(o, op, raw, sc, tid);
+        else
+            transform_tile<ROWS, false, false>(o, op, raw, sc, tid);
+    }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(320, 1)
+    umma_dq_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
+                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                        const __grid_constant__ CUtensorMap tmXs, const __grid_constant__ CUtensorMap tmYs,
+                        const __grid_constant__ GemmKernelParams P) {
+    using Cfg = DqCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int S = P.stages;
+    uint8_t* ring = smem;
+    float* staging = reinterpret_cast<float*>(smem + (size_t)S * Cfg::STAGE_BYTES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * Cfg::STAGE_BYTES + Cfg::STAGING_BYTES);
+    uint64_t* ready = full + Cfg::MAX_STAGES;
+    uint64_t* empty = ready + Cfg::MAX_STAGES;
+    uint64_t* tfull = empty + Cfg::MAX_STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* done = tempty + 2;
+    uint64_t* cbar = done + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cbar + EPI_CBARS);
+    volatile uint32_t* bcast = tmem_slot + 1;
+    volatile uint32_t* abort_flag = tmem_slot + 2;
+
+    const DqParams& dq = P.dq;
+    const uint32_t x_bytes = (dq.x.int4 ? Cfg::X_RAW : Cfg::X_OP) + (dq.x.has_scale ? BM * 2 * dq.x.sc_rows : 0);
+    const uint32_t y_bytes = (dq.y.int4 ? Cfg::Y_RAW : Cfg::Y_OP) + (dq.y.has_scale ? BN * 2 * dq.y.sc_rows : 0);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&ready[s], 128);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 128);
+        }
+        mbar_init(done, 1);
+        for (int i = 0; i < EPI_CBARS; ++i) mbar_init(&cbar[i], 1);
+        *bcast = 0;
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmY);
+        if (P.dq.x.has_scale) tma_prefetch_desc(&tmXs);
+        if (P.dq.y.has_scale) tma_prefetch_desc(&tmYs);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const Guard g{P.status, P.timeout_ns, abort_flag};
+
+    auto x_op = [&](int s) { return ring + (size_t)s * Cfg::STAGE_BYTES; };
+    auto y_op = [&](int s) { return x_op(s) + Cfg::X_OP; };
+    auto x_raw = [&](int s) { return y_op(s) + Cfg::Y_OP; };
+    auto y_raw = [&](int s) { return x_raw(s) + Cfg::X_RAW; };
+    auto x_sc = [&](int s) { return y_raw(s) + Cfg::Y_RAW; };
+    auto y_sc = [&](int s) { return x_sc(s) + Cfg::X_SC; };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            WorkIter w;
+            w.init(P.sched, blockIdx.x);
+            Unit u;
+            int s = 0;
+            uint32_t ph = 0, armed = 0, armed_par = 0;
+            bool ok = true;
+            while (ok && w.next(P.sched, blockIdx.x, BM, BN, u)) {
+                for (int k = u.k_begin; k < u.k_end; ++k) {
+                    if (!wait_bar(&empty[s], ph ^ 1, g, SITE_PRODUCER_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[s], x_bytes + y_bytes);
+                    // int4 tiles are addressed in bytes: K-step k starts at byte k*32
+                    if (dq.x.int4)
+                        tma_load_2d(x_raw(s), &tmX, &full[s], k * (BK / 2), (int32_t)u.x_row0);
+                    else
+                        tma_load_2d(x_op(s), &tmX, &full[s], k * BK, (int32_t)u.x_row0);
+                    if (dq.y.int4)
+                        tma_load_2d(y_raw(s), &tmY, &full[s], k * (BK / 2), (int32_t)u.y_row0);
+                    else
+                        tma_load_2d(y_op(s), &tmY, &full[s], k * BK, (int32_t)u.y_row0);
+                    // the scale rows of this K-step: groups (k*64)/group .. + sc_rows - 1
+                    if (dq.x.has_scale)
+                        tma_load_2d(x_sc(s), &tmXs, &full[s], (int32_t)u.x_row0, (k * BK) / dq.x.group);
+                    if (dq.y.has_scale)
+                        tma_load_2d(y_sc(s), &tmYs, &full[s], (int32_t)u.y_row0, (k * BK) / dq.y.group);
+                    armed |= 1u << s;
+                    armed_par = (armed_par & ~(1u << s)) | (ph << s);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            for (int i = 0; i < S; ++i)
+                if (armed & (1u << i)) wait_bar_drain(&full[i], (armed_par >> i) & 1u, g);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            WorkIter w;
+            w.init(P.sched, blockIdx.x);
+            Unit u;
+            int s = 0;
+            uint32_t ph = 0, acc_it = 0;
+            bool ok = true, issued = false;
+            while (ok && w.next(P.sched, blockIdx.x, BM, BN, u)) {
+                const int buf = acc_it & 1;
+                const uint32_t aph = (acc_it >> 1) & 1;
+                ++acc_it;
+                if (!wait_bar(&tempty[buf], aph ^ 1, g, SITE_MMA_TMEM_EMPTY)) break;
+                tc_fence_after_sync();
+                const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+                for (int k = u.k_begin; k < u.k_end; ++k) {
+                    if (!wait_bar(&ready[s], ph, g, SITE_MMA_OPERAND)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t ad = make_sw128_kmajor_desc(smem_u32(x_op(s)));
+                    const uint64_t bd = make_sw128_kmajor_desc(smem_u32(y_op(s)));
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                        umma_f16_ss(d, ad + 2 * kk, bd + 2 * kk, P.idesc, (k > u.k_begin || kk > 0) ? 1u : 0u);
+                    issued = true;
+                    umma_commit(&empty[s]);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&tfull[buf]);
+            }
+            if (issued) {
+                umma_commit(done);
+                wait_bar_drain(done, 0, g);
+            }
+        }
+    } else if (warp < 6) {
+        epilogue<BN>(P, &tmC, &tmD, tmem_base, tfull, tempty, reinterpret_cast<uint8_t*>(staging), cbar, bcast, g);
+    } else {
+        // transform warps
+        const int tid = threadIdx.x - 192;
+        WorkIter w;
+        w.init(P.sched, blockIdx.x);
+        Unit u;
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        while (ok && w.next(P.sched, blockIdx.x, BM, BN, u)) {
+            for (int k = u.k_begin; k < u.k_end; ++k) {
+                if (!wait_bar(&full[s], ph, g, SITE_DQ_RAW)) {
+                    ok = false;
+                    break;
+                }
+                if (dq.x.active) transform_any<BM>(dq.x, x_op(s), x_raw(s), x_sc(s), dq.out_bf16, tid);
+                if (dq.y.active) transform_any<BN>(dq.y, y_op(s), y_raw(s), y_sc(s), dq.out_bf16, tid);
+                fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+                mbar_arrive(&ready[s]);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+template <int BN>
+cudaError_t launch_dq_bn(const GemmMaps& m, const GemmKernelParams& p, int grid, cudaStream_t st) {
+    const size_t smem = DqCfg<BN>::smem_bytes(p.stages);
+    // raise the dynamic shared-memory limit once per device (to the largest ring)
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load() & bit)) {
+        e = cudaFuncSetAttribute(umma_dq_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)DqCfg<BN>::smem_bytes(DqCfg<BN>::max_stages()));
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit);
+    }
+    umma_dq_gemm_kernel<BN><<<grid, 320, smem, st>>>(m.x, m.y, m.c, m.d, m.xs, m.ys, p);
+    return cudaGetLastError();
+}
+
+template <int BN>
+int dq_stages_bn() {
+    return DqCfg<BN>::max_stages();
+}
+
+}  // namespace qg

@@ -1,0 +1,9 @@
+// Instantiations of the scaled-operand tcgen05 GEMM kernel for tile widths 128, 256.
+#include "umma_dq_gemm.cuh"
+
+namespace qg {
+template cudaError_t launch_dq_bn<128>(const GemmMaps&, const GemmKernelParams&, int, cudaStream_t);
+template int dq_stages_bn<128>();
+template cudaError_t launch_dq_bn<256>(const GemmMaps&, const GemmKernelParams&, int, cudaStream_t);
+template int dq_stages_bn<256>();
+}  // namespace qg

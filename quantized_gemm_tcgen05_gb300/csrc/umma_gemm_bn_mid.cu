@@ -1,0 +1,10 @@
+// Instantiations of the dense tcgen05 GEMM kernel for tile widths 128, 192
+// (separate translation units so they compile in parallel).
+#include "umma_gemm.cuh"
+
+namespace qg {
+template cudaError_t launch_umma_bn<128>(const GemmMaps&, const GemmKernelParams&, int, cudaStream_t);
+template int umma_stages_bn<128>();
+template cudaError_t launch_umma_bn<192>(const GemmMaps&, const GemmKernelParams&, int, cudaStream_t);
+template int umma_stages_bn<192>();
+}  // namespace qg

@@ -138,3 +138,20 @@ def test_config2_full_schedules_sampled(lib, sched):
     ii, jj = sample_indices(p.M, p.N, 1500, seed=6)
     ref, bound = oracle.gemm_entries(p, ii, jj)
     assert_close(D.double().cpu().numpy()[ii, jj], ref, bound, p.d_type, f"C2 {sched}")
+
+
+@pytest.mark.parametrize("kernel", ["umma_bn16_swap/dp", "umma_bn32_swap/splitk3", "umma_bn64_swap/streamk",
+                                    "umma_bn128_swap/dp", "umma_bn16/dp", "umma_bn32/streamk", "umma_bn64/dp",
+                                    "umma_bn128/splitk2", "umma_bn192/dp", "umma_bn192/streamk", "umma_bn224/dp",
+                                    "umma_bn224/splitk3", "umma_bn256/streamk"])
+def test_every_registered_kernel(lib, kernel, monkeypatch):
+    # every tile width and schedule the registry can dispatch, pinned by
+    # GEMM_FORCE_KERNEL, on a ragged problem that spans several tiles
+    monkeypatch.setenv("GEMM_FORCE_KERNEL", kernel)
+    swap = "_swap" in kernel
+    M = 70 if swap else 300
+    p = synth.dense(M, 520, 200 + 64 * 5, seed=len(kernel), a_type=synth.BF16, d_type=synth.BF16, alpha=1.5,
+                    beta=0.5, dist="normal", scale=0.1)
+    _check(lib, p, what=kernel)
+    import quantized_gemm_tcgen05_gb300 as qg
+    assert qg.gemm_last_choice(lib.h) == kernel
