@@ -44,6 +44,7 @@ struct gemm_handle {
         bool valid;
     };
     MapEntry maps[128] = {};
+    int pair_clusters = -1;  // clusters of two the CTA-pair kernel can keep resident (queried once)
     const void* dev_ptrs[64] = {};
     int dev_ptr_next = 0;
 };
@@ -244,10 +245,22 @@ int make_map_scale(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t type
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+// Programs a choice can use: SMs, or for the CTA pair twice the resident clusters.
+int capacity(gemm_handle* h, const Choice& c) {
+    if (!c.pair) return h->sm_count;
+    if (h->pair_clusters < 0) {
+        const int n = umma_pair_max_clusters(256);
+        h->pair_clusters = n > 0 ? n : 0;
+    }
+    const int cap = 2 * h->pair_clusters;
+    return cap < h->sm_count ? cap : h->sm_count;
+}
+
 int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_workspace_t* ws, cudaStream_t st) {
     GemmKernelParams kp;
     memset(&kp, 0, sizeof kp);
-    kp.sched = make_sched(p, c, h->sm_count);
+    if (c.pair && capacity(h, c) < 2) return GEMM_ERR_NO_KERNEL;
+    kp.sched = make_sched(p, c, capacity(h, c));
     const size_t need_p = partials_bytes_needed(kp.sched, c.bn);
     const size_t need_c = counters_bytes_needed(kp.sched);
     if (need_p || need_c) {
@@ -296,9 +309,11 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
         kp.x3d = kp.y3d = 0;
     } else {
         rc = make_map(h, &tx, p.A, p.a_type, p.K, p.M, p.lda, p.batches, p.a_bs, 128);
+        // the CTA pair loads half of the Y tile in each CTA
+        const int32_t y_box = c.pair ? c.bn / 2 : c.bn;
         if (rc == GEMM_OK)
             rc = s4 ? make_map_s4(h, &ty, p.B, p.K, p.N, p.ldb, c.bn)
-                    : make_map(h, &ty, p.B, p.b_type, p.K, p.N, p.ldb, p.batches, p.b_bs, c.bn);
+                    : make_map(h, &ty, p.B, p.b_type, p.K, p.N, p.ldb, p.batches, p.b_bs, y_box);
         kp.x3d = kp.y3d = p.batches > 1;
     }
     if (rc != GEMM_OK) return rc;
@@ -311,9 +326,11 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
         const char* et = getenv("GEMM_EPI_TMA");
         const bool allowed = !(et && et[0] == '0');
         e.tma = allowed && !c.swap && p.family != FAM_GROUPED && c.bn >= 32 && ok16(p.D, p.ldd, p.d_bs) &&
-                (e.C == nullptr || ok16(p.C, p.ldc, p.c_bs));
+                (e.C == nullptr || ok16(p.C, p.ldc, p.c_bs)) && !(c.pair && es == 4);
         if (e.tma) {
-            e.ncb = es == 2 ? 4 : 2;
+            // buffers per epilogue warp: 32 KB of epilogue shared memory (16 KB
+            // in the CTA-pair kernel) split over 4 warps
+            e.ncb = c.pair ? 2 : (es == 2 ? 4 : 2);
             rc = make_map_cd(h, &maps.d, p.D, p.d_type, p.M, p.N, p.ldd, p.batches, p.d_bs);
             if (rc == GEMM_OK && e.C) rc = make_map_cd(h, &maps.c, p.C, p.d_type, p.M, p.N, p.ldc, p.batches, p.c_bs);
             if (rc != GEMM_OK) return rc;
@@ -357,18 +374,24 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
         cudaError_t ce = launch_umma_dq_gemm(c.bn, maps, kp, kp.sched.programs, st);
         return ce == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
-    kp.stages = umma_max_stages(c.bn);
+    kp.stages = c.pair ? umma_pair_max_stages(c.bn) : umma_max_stages(c.bn);
     if (kp.stages < 2) return GEMM_ERR_NO_KERNEL;
     if (const char* fs = getenv("GEMM_STAGES")) {  // ring depth override for tuning sweeps
         const int want = atoi(fs);
         if (want >= 2 && want < kp.stages) kp.stages = want;
+    }
+    if (c.pair) {
+        kp.pair = 1;
+        kp.idesc = make_idesc_f16(p.a_type == GEMM_BF16, 256, c.bn);
+        cudaError_t ce = launch_umma_pair_gemm(c.bn, maps, kp, 2 * kp.sched.programs, st);
+        return ce == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
     cudaError_t ce = launch_umma_gemm(c.bn, maps, kp, kp.sched.programs, st);
     return ce == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 bool workspace_fits(gemm_handle* h, const Problem& p, const Choice& c, const gemm_workspace_t* ws) {
-    SchedParams s = make_sched(p, c, h->sm_count);
+    SchedParams s = make_sched(p, c, capacity(h, c));
     const size_t need_p = partials_bytes_needed(s, c.bn), need_c = counters_bytes_needed(s);
     if (!need_p && !need_c) return true;
     return ws && ws->partials && ws->barriers && ws->partials_size >= need_p && ws->barriers_size >= need_c;
@@ -412,6 +435,7 @@ bool forced_kernel(const Problem& p, Choice* out) {
     Choice c;
     c.bn = atoi(bn + 2);
     c.swap = strstr(f, "_swap") != nullptr && strstr(f, "_swap") < slash;
+    c.pair = strncmp(f, "umma2_", 6) == 0;
     if (strncmp(slash + 1, "dp", 2) == 0) {
         c.sched = SCHED_DP;
     } else if (strncmp(slash + 1, "streamk", 7) == 0) {
@@ -426,6 +450,9 @@ bool forced_kernel(const Problem& p, Choice* out) {
         return false;
     if (p.family == FAM_DQ && (c.bn == 192 || c.bn == 224)) return false;
     if (c.swap && (p.family == FAM_GROUPED || p.batches != 1)) return false;
+    if (c.pair && (p.family != FAM_DENSE || c.swap || c.sched != SCHED_DP ||
+                   !(c.bn == 128 || c.bn == 224 || c.bn == 256)))
+        return false;
     if (p.family == FAM_GROUPED) c.sched = SCHED_DP;
     *out = c;
     return true;

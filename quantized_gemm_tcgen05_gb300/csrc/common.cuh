@@ -77,6 +77,24 @@ __device__ __forceinline__ bool wait_bar_drain(uint64_t* bar, uint32_t parity, c
 
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// ---- unit iteration shared by all roles ----------------------------------------
+//
+// A 1-CTA kernel walks 128-row tiles with program id blockIdx.x.  The CTA-pair
+// kernel walks 256-row tiles with program id = cluster id; each CTA of the
+// pair owns 128 of the rows (the odd CTA the upper half).
+
+__device__ __forceinline__ int unit_pid(const GemmKernelParams& P) {
+    return P.pair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+}
+
+__device__ __forceinline__ bool next_unit(const GemmKernelParams& P, WorkIter& w, Unit& u, int bn) {
+    if (!P.pair) return w.next(P.sched, (int)blockIdx.x, BM, bn, u);
+    if (!w.next(P.sched, (int)(blockIdx.x >> 1), 2 * BM, bn, u)) return false;
+    u.x_row0 += (int64_t)(blockIdx.x & 1) * BM;
+    u.x_rows = BM;
+    return true;
+}
+
 // ---- element access ------------------------------------------------------------------
 
 __device__ __forceinline__ float ld_elem(const void* p, int32_t t, int64_t i) {
@@ -279,10 +297,10 @@ __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uin
     const int r = ew * 32 + lane;
     float4* staging = reinterpret_cast<float4*>(staging_all) + ew * 32 * CK::Q;
     WorkIter w;
-    w.init(P.sched, blockIdx.x);
+    w.init(P.sched, unit_pid(P));
     Unit u;
     uint32_t acc_it = 0;
-    while (w.next(P.sched, blockIdx.x, BM, BN, u)) {
+    while (next_unit(P, w, u, BN)) {
         const int buf = acc_it & 1;
         const uint32_t aph = (acc_it >> 1) & 1;
         ++acc_it;
@@ -376,15 +394,15 @@ struct ChunkStream {
     Unit u;
     int c;
     bool valid;
-    __device__ __forceinline__ void init(const SchedParams& s, int pid, int bn) {
-        w.init(s, pid);
+    __device__ __forceinline__ void init(const GemmKernelParams& P, int bn) {
+        w.init(P.sched, unit_pid(P));
         c = 0;
-        valid = w.next(s, pid, BM, bn, u);
+        valid = next_unit(P, w, u, bn);
     }
-    __device__ __forceinline__ void advance(const SchedParams& s, int pid, int bn, int nch) {
+    __device__ __forceinline__ void advance(const GemmKernelParams& P, int bn, int nch) {
         if (++c == nch) {
             c = 0;
-            valid = w.next(s, pid, BM, bn, u);
+            valid = next_unit(P, w, u, bn);
         }
     }
 };
@@ -413,7 +431,6 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
     uint8_t* ebuf = ebuf_all + (size_t)ew * ncb * buf_bytes;
     uint64_t* cbar = cbar_all + ew * 4;
     const bool use_c = e.beta != 0.0f;
-    const int pid = blockIdx.x;
 
     auto slab_x = [&](const Unit& u, int c) { return (int32_t)(u.y_row0 + c * W); };
     auto slab_y = [&](const Unit& u) { return (int32_t)(u.x_row0 + ew * 32); };
@@ -438,7 +455,7 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
     };
 
     ChunkStream pre;
-    pre.init(P.sched, pid, BN);
+    pre.init(P, BN);
     uint32_t ppos = 0, gpos = 0;
     auto issue_c = [&]() {
         const int b = ppos % ncb;
@@ -449,7 +466,7 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
             else
                 tma_load_2d(ebuf + b * buf_bytes, tmC, &cbar[b], slab_x(pre.u, pre.c), slab_y(pre.u));
         }
-        pre.advance(P.sched, pid, BN, NCH);
+        pre.advance(P, BN, NCH);
         ++ppos;
     };
     if (use_c)
@@ -533,10 +550,10 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
     };
 
     WorkIter w;
-    w.init(P.sched, pid);
+    w.init(P.sched, unit_pid(P));
     Unit u;
     uint32_t acc_it = 0;
-    while (ok && w.next(P.sched, pid, BM, BN, u)) {
+    while (ok && next_unit(P, w, u, BN)) {
         const int buf = acc_it & 1;
         const uint32_t aph = (acc_it >> 1) & 1;
         ++acc_it;

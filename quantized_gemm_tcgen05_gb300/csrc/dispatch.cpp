@@ -62,9 +62,10 @@ SchedParams make_sched(const Problem& p, const Choice& c, int sm_count) {
         s.tiles_x = (int32_t)ceil_div(p.N, 128);
         s.tiles_y = (int32_t)ceil_div(p.M, c.bn);
     } else {
-        s.tiles_x = (int32_t)ceil_div(p.M, 128);
+        s.tiles_x = (int32_t)ceil_div(p.M, c.pair ? 256 : 128);
         s.tiles_y = (int32_t)ceil_div(p.N, c.bn);
     }
+    if (c.pair) sm_count /= 2;  // programs are clusters of two CTAs
     const int64_t T = total_tiles(s);
     s.splits = 1;
     s.chunk = s.k_iters;
@@ -153,6 +154,14 @@ std::vector<Choice> candidates(const Problem& p, int sm_count) {
     if (p.N > 128)
         for (int32_t bn : {192, 224, 256}) add_scheds(bn, 0);
     if (swap_allowed(p)) add_scheds(swap_bn(p.M), 1);
+    if (p.family == FAM_DENSE && p.M > 128)
+        for (int32_t bn : {128, 224, 256}) {
+            Choice c;
+            c.bn = bn;
+            c.pair = 1;
+            c.sched = SCHED_DP;
+            out.push_back(c);
+        }
     return out;
 }
 
@@ -171,16 +180,27 @@ Choice heuristic(const Problem& p, int sm_count) {
         c.bn = 256;  // measured best for ragged MoE blocks (the tile count is only an upper bound)
     } else {
         // the tile width that minimises waves x width (time per wave grows
-        // with the width); wider wins ties
+        // with the width); wider wins ties.  256-row tiles on CTA pairs (half
+        // the Y-operand bytes per SM) whenever they fill at least one wave of
+        // clusters: a wave of pairs covers as many rows as a wave of single
+        // CTAs and measured about 20% faster.
         int64_t best = -1;
-        for (int32_t bn : {256, 224, 192, 128}) {
-            Choice t;
-            t.bn = bn;
-            const int64_t T = total_tiles(make_sched(p, t, sm_count));
-            const int64_t cost = ceil_div(T, sm_count) * bn;
-            if (best < 0 || cost < best) {
-                best = cost;
-                c.bn = bn;
+        for (int32_t pair : {1, 0}) {
+            if (pair && (p.family != FAM_DENSE || p.M <= 128)) continue;
+            const int64_t cap = pair ? sm_count / 2 : sm_count;
+            for (int32_t bn : {256, 224, 192, 128}) {
+                if (pair && bn == 192) continue;
+                Choice t;
+                t.bn = bn;
+                t.pair = pair;
+                const int64_t T = total_tiles(make_sched(p, t, sm_count));
+                if (pair && T < cap) continue;
+                const int64_t cost = ceil_div(T, cap) * bn * (pair ? 8 : 10);
+                if (best < 0 || cost < best) {
+                    best = cost;
+                    c.bn = bn;
+                    c.pair = pair;
+                }
             }
         }
     }
@@ -202,7 +222,8 @@ Choice heuristic(const Problem& p, int sm_count) {
 
 std::string choice_name(const Problem& p, const Choice& c) {
     char buf[96];
-    const char* fam = p.family == FAM_DQ ? "umma_dq" : (p.family == FAM_GROUPED ? "umma_grouped" : "umma");
+    const char* fam =
+        p.family == FAM_DQ ? "umma_dq" : (p.family == FAM_GROUPED ? "umma_grouped" : (c.pair ? "umma2" : "umma"));
     const char* sk = c.sched == SCHED_DP ? "dp" : (c.sched == SCHED_STREAMK ? "streamk" : "splitk");
     if (c.sched == SCHED_SPLITK)
         snprintf(buf, sizeof buf, "%s_bn%d%s/%s%d", fam, c.bn, c.swap ? "_swap" : "", sk, c.splits);
@@ -213,10 +234,10 @@ std::string choice_name(const Problem& p, const Choice& c) {
 
 // ---- cache text format ------------------------------------------------------------
 //
-//   qgemm-dispatch-cache 1
+//   qgemm-dispatch-cache 2
 //   device <name, spaces as '_'> sm <count> cc <major*10+minor>
 //   entries <n>
-//   <family> <a> <b> <d> <has_c> <has_u> <has_v> <ga> <gb> <m_bucket> <N> <K> <batches> : <bn> <swap> <sched> <splits> <us>
+//   <family> <a> <b> <d> <has_c> <has_u> <has_v> <ga> <gb> <m_bucket> <N> <K> <batches> : <bn> <swap> <sched> <splits> <pair> <us>
 //   ...
 //   end
 
@@ -229,7 +250,7 @@ static std::string sanitize(const std::string& s) {
 
 std::string cache_serialize(const std::map<Key, Choice>& cache, const std::string& device, int sm, int cc) {
     std::ostringstream os;
-    os << "qgemm-dispatch-cache 1\n";
+    os << "qgemm-dispatch-cache 2\n";
     os << "device " << sanitize(device) << " sm " << sm << " cc " << cc << "\n";
     os << "entries " << cache.size() << "\n";
     for (const auto& kv : cache) {
@@ -239,7 +260,8 @@ std::string cache_serialize(const std::map<Key, Choice>& cache, const std::strin
         snprintf(us, sizeof us, "%.3f", c.us);
         os << k.family << ' ' << k.a_type << ' ' << k.b_type << ' ' << k.d_type << ' ' << k.has_c << ' ' << k.has_u
            << ' ' << k.has_v << ' ' << k.ga << ' ' << k.gb << ' ' << k.m_bucket << ' ' << k.N << ' ' << k.K << ' '
-           << k.batches << " : " << c.bn << ' ' << c.swap << ' ' << c.sched << ' ' << c.splits << ' ' << us
+           << k.batches << " : " << c.bn << ' ' << c.swap << ' ' << c.sched << ' ' << c.splits << ' ' << c.pair << ' '
+           << us
            << "\n";
     }
     os << "end\n";
@@ -250,6 +272,9 @@ static bool valid_choice(const Key& k, const Choice& c) {
     const bool bn_ok = c.bn == 16 || c.bn == 32 || c.bn == 64 || c.bn == 128 || c.bn == 192 || c.bn == 224 || c.bn == 256;
     if (!bn_ok || (c.swap != 0 && c.swap != 1) || c.sched < SCHED_DP || c.sched > SCHED_STREAMK) return false;
     if (c.splits < 1 || c.splits > 64 || !(c.us >= 0.0f)) return false;
+    if (c.pair != 0 && c.pair != 1) return false;
+    if (c.pair && (c.swap || c.sched != SCHED_DP || k.family != FAM_DENSE)) return false;
+    if (c.pair && c.bn != 128 && c.bn != 224 && c.bn != 256) return false;
     if (k.family < FAM_DENSE || k.family > FAM_GROUPED) return false;
     if (k.N < 0 || k.K < 0 || k.m_bucket < 1 || k.batches < 1) return false;
     return true;
@@ -260,7 +285,7 @@ bool cache_parse(const std::string& text, const std::string& device, int sm, int
     std::string magic, word, dev;
     int version = 0, sm_in = -1, cc_in = -1;
     long long n = -1;
-    if (!(is >> magic >> version) || magic != "qgemm-dispatch-cache" || version != 1) return false;
+    if (!(is >> magic >> version) || magic != "qgemm-dispatch-cache" || version != 2) return false;
     if (!(is >> word) || word != "device" || !(is >> dev)) return false;
     if (!(is >> word) || word != "sm" || !(is >> sm_in)) return false;
     if (!(is >> word) || word != "cc" || !(is >> cc_in)) return false;
@@ -273,7 +298,7 @@ bool cache_parse(const std::string& text, const std::string& device, int sm, int
         std::string colon;
         long long mb, N, K;
         if (!(is >> k.family >> k.a_type >> k.b_type >> k.d_type >> k.has_c >> k.has_u >> k.has_v >> k.ga >> k.gb >>
-              mb >> N >> K >> k.batches >> colon >> c.bn >> c.swap >> c.sched >> c.splits >> c.us))
+              mb >> N >> K >> k.batches >> colon >> c.bn >> c.swap >> c.sched >> c.splits >> c.pair >> c.us))
             return false;
         if (colon != ":") return false;
         k.m_bucket = mb;

@@ -40,6 +40,7 @@ struct Choice {
     int32_t swap = 0;    // X = B, Y = A (D^T = B^T A^T), for small M
     int32_t sched = 0;   // SchedKind
     int32_t splits = 1;  // split-K slices (SCHED_SPLITK)
+    int32_t pair = 0;    // CTA-pair kernel: 256 x bn tiles over clusters of two SMs
     float us = 0.0f;     // measured time, 0 if never measured
 };
 
@@ -58,6 +59,7 @@ int64_t m_bucket(int64_t M);
 Key make_key(const Problem& p);
 
 // Tiles of a problem under a choice, and the schedule parameters.
+// sm_count: SMs of the device; the CTA-pair kernel runs on clusters of two.
 SchedParams make_sched(const Problem& p, const Choice& c, int sm_count);
 size_t partials_bytes_needed(const SchedParams& s, int bn);
 size_t counters_bytes_needed(const SchedParams& s);

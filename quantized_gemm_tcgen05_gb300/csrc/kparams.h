@@ -72,6 +72,7 @@ struct GemmKernelParams {
     int32_t* counters;    // per-tile arrival counters (self-resetting)
     uint32_t* status;     // device status words [4]
     uint64_t timeout_ns;  // bound on every wait
+    int32_t pair;         // CTA-pair kernel: units are 256-row tiles shared by the two CTAs of a cluster
 };
 
 // Instruction descriptor of tcgen05.mma.kind::f16: fp32 accumulator (bits
@@ -85,6 +86,7 @@ QG_HD uint32_t make_idesc_f16(int ab_is_bf16, int m, int n) {
 // Tile widths (UMMA N) instantiated for each kernel.
 #define QG_FOR_EACH_DENSE_BN(X) X(16) X(32) X(64) X(128) X(192) X(224) X(256)
 #define QG_FOR_EACH_DQ_BN(X) X(16) X(32) X(64) X(128) X(256)
+#define QG_FOR_EACH_PAIR_BN(X) X(128) X(224) X(256)
 
 // Entry points implemented in the .cu files.
 // The four tensor maps of one launch: X and Y operands, C and D (the last two
@@ -104,6 +106,12 @@ template <int BN>
 cudaError_t launch_dq_bn(const GemmMaps& m, const GemmKernelParams& p, int grid, cudaStream_t st);
 template <int BN>
 int dq_stages_bn();
+template <int BN>
+cudaError_t launch_pair_bn(const GemmMaps& m, const GemmKernelParams& p, int grid, cudaStream_t st);
+template <int BN>
+int pair_stages_bn();
+template <int BN>
+int pair_max_clusters_bn();
 
 cudaError_t launch_umma_gemm(int bn, const GemmMaps& maps, const GemmKernelParams& p, int grid, cudaStream_t st);
 cudaError_t launch_umma_dq_gemm(int bn, const GemmMaps& maps, const GemmKernelParams& p, int grid,
@@ -111,6 +119,9 @@ cudaError_t launch_umma_dq_gemm(int bn, const GemmMaps& maps, const GemmKernelPa
 cudaError_t launch_scale_c(const EpiParams& e, int64_t batches, cudaStream_t st);
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t timeout_ns, cudaStream_t st);
 int umma_max_stages(int bn);
+cudaError_t launch_umma_pair_gemm(int bn, const GemmMaps& maps, const GemmKernelParams& p, int grid, cudaStream_t st);
+int umma_pair_max_stages(int bn);
+int umma_pair_max_clusters(int bn);
 int umma_dq_max_stages(int bn);
 cudaError_t device_status_ptr(uint32_t** out);
 

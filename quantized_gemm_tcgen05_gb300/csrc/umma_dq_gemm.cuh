@@ -2,7 +2,7 @@
 // group-wise scaling (the U/V scale operands that advance at K-group
 // boundaries, "InternLM Lmdeploy Gemm MainloopSm80V2", section Description).
 //
-// Same persistent warp-specialised structure as the dense kernel, plus four
+// Same persistent warp-specialised structure as the dense kernel, plus eight
 // transform warps between the TMA ring and the tensor core:
 //
 //   warp 0      TMA: X tile (128 x 64 16-bit, SWIZZLE_128B, or 128 x 32 bytes
@@ -10,7 +10,7 @@
 //               of int4) into stage s, arming full[s].
 //   warp 1      TMEM owner / MMA issuer; waits ready[s], not full[s].
 //   warps 2-5   epilogue (shared with the dense kernel).
-//   warps 6-9   transform: wait full[s]; for every 16-byte chunk of 8 K
+//   warps 6-13  transform: wait full[s]; for every 16-byte chunk of 8 K
 //               values of a transformed operand, form RN(x * scale) in fp32
 //               and write the chunk where the SWIZZLE_128B canonical layout
 //               wants it; fence the writes to the async proxy; arrive ready[s].
@@ -60,14 +60,19 @@ __device__ __forceinline__ float2 unpack2(uint32_t w, int is_bf16) {
     return __half22float2(*reinterpret_cast<__half2*>(&w));
 }
 
-// Chunk i of a transform thread covers 16-byte chunk c = tid + 128*i of a
+// Chunk i of a transform thread covers 16-byte chunk c = tid + XF_THREADS*i of a
 // ROWS x 64 tile: row c/8 and logical K-chunk j (8 values at k0 + 8j).  For a
 // packed int4 operand j = c % 8 (the destination is permuted); for a 16-bit
 // operand already in the swizzled layout the physical chunk is c % 8 and the
 // logical one is (c % 8) ^ (row % 8).
+// Transform threads per CTA: eight warps, two per SM sub-partition, so the
+// dependent integer/float chains of one warp hide behind the other's.
+constexpr int XF_THREADS = 256;
+
 template <int ROWS>
 struct XformChunks {
-    static constexpr int N = ROWS / 16;  // chunks per transform thread
+    static constexpr int TOTAL = ROWS * 8;  // 16-byte chunks in a ROWS x 64 tile
+    static constexpr int N = (TOTAL + XF_THREADS - 1) / XF_THREADS;  // per transform thread
 };
 
 // Scale of row r for logical K-chunk j, from the stage's scale rows
@@ -107,7 +112,8 @@ __device__ __forceinline__ void transform_tile(const OperandXform& o, uint8_t* o
     uint4 in[NC];
 #pragma unroll
     for (int i = 0; i < NC; ++i) {
-        const int c = tid + 128 * i;
+        const int c = tid + XF_THREADS * i;
+        if (XformChunks<ROWS>::TOTAL % XF_THREADS != 0 && c >= XformChunks<ROWS>::TOTAL) break;
         const int r = c >> 3;
         const int j = INT4 ? (c & 7) : ((c & 7) ^ (r & 7));
         s[i] = stage_scale<ROWS>(o, sc, r, j);
@@ -118,7 +124,8 @@ __device__ __forceinline__ void transform_tile(const OperandXform& o, uint8_t* o
     }
 #pragma unroll
     for (int i = 0; i < NC; ++i) {
-        const int c = tid + 128 * i;
+        const int c = tid + XF_THREADS * i;
+        if (XformChunks<ROWS>::TOTAL % XF_THREADS != 0 && c >= XformChunks<ROWS>::TOTAL) break;
         const int r = c >> 3;
         uint4 out;
         if constexpr (INT4) {
@@ -167,7 +174,7 @@ __device__ __forceinline__ void transform_any(const OperandXform& o, uint8_t* op
 }
 
 template <int BN>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(192 + XF_THREADS, 1)
     umma_dq_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                         const __grid_constant__ CUtensorMap tmXs, const __grid_constant__ CUtensorMap tmYs,
@@ -197,7 +204,7 @@ __global__ void __launch_bounds__(320, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&ready[s], 128);
+            mbar_init(&ready[s], XF_THREADS);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -367,7 +374,7 @@ cudaError_t launch_dq_bn(const GemmMaps& m, const GemmKernelParams& p, int grid,
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
-    umma_dq_gemm_kernel<BN><<<grid, 320, smem, st>>>(m.x, m.y, m.c, m.d, m.xs, m.ys, p);
+    umma_dq_gemm_kernel<BN><<<grid, 192 + XF_THREADS, smem, st>>>(m.x, m.y, m.c, m.d, m.xs, m.ys, p);
     return cudaGetLastError();
 }
 

@@ -57,6 +57,36 @@ int umma_max_stages(int bn) {
     }
 }
 
+cudaError_t launch_umma_pair_gemm(int bn, const GemmMaps& m, const GemmKernelParams& p, int grid, cudaStream_t st) {
+    switch (bn) {
+#define QG_CASE(B) \
+    case B: return launch_pair_bn<B>(m, p, grid, st);
+        QG_FOR_EACH_PAIR_BN(QG_CASE)
+#undef QG_CASE
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+int umma_pair_max_stages(int bn) {
+    switch (bn) {
+#define QG_CASE(B) \
+    case B: return pair_stages_bn<B>();
+        QG_FOR_EACH_PAIR_BN(QG_CASE)
+#undef QG_CASE
+        default: return 0;
+    }
+}
+
+int umma_pair_max_clusters(int bn) {
+    switch (bn) {
+#define QG_CASE(B) \
+    case B: return pair_max_clusters_bn<B>();
+        QG_FOR_EACH_PAIR_BN(QG_CASE)
+#undef QG_CASE
+        default: return 0;
+    }
+}
+
 cudaError_t launch_scale_c(const EpiParams& e, int64_t batches, cudaStream_t st) {
     int64_t total = batches * e.M * e.N;
     int grid = (int)((total + 255) / 256);
