@@ -39,6 +39,26 @@ import synth  # noqa: E402
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# ---- multi-rank aggregation -----------------------------------------------------------
+
+def max_over_ranks(ms, dist, device="cuda"):
+    """The largest of the ranks' timings (every rank gets it); `ms` itself
+    when there is no process group."""
+    if dist is None:
+        return float(ms)
+    import torch
+
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(unit_per_step, steps, world, ms):
+    """Whole-job throughput: every rank runs `steps` steps of `unit_per_step`
+    units each; the job takes the slowest rank's `ms`."""
+    return world * unit_per_step * steps / (ms / 1e3)
+
+
 # ---- workloads ----------------------------------------------------------------------
 
 WORKLOADS = {
@@ -330,12 +350,9 @@ def run_ours(args, rank, world, cfg):
         total_ms = start.elapsed_time(end)
         launch_ms = [a.elapsed_time(b) for a, b in evs]
     sampler.stop()
-    if dist is not None:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist)
     ms_per_step = total_ms / args.steps
-    value = world * unit_per_step * args.steps / (total_ms / 1e3)
+    value = job_throughput(unit_per_step, args.steps, world, total_ms)
     if qg.gemm_device_status(R.h, R.stream):
         raise RuntimeError("device status reported a timeout during the timed region")
 
@@ -424,12 +441,8 @@ def measure_e2e(R, torch, unit_per_step, unit, world, dist, steps):
         step()
     e.record(stream)
     torch.cuda.synchronize()
-    ms = s.elapsed_time(e)
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": round(world * unit_per_step * steps / (ms / 1e3), 3), "unit": unit,
+    ms = max_over_ranks(s.elapsed_time(e), dist)
+    return {"value": round(job_throughput(unit_per_step, steps, world, ms), 3), "unit": unit,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms / steps, 4)}
 
 
