@@ -126,28 +126,39 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(files=None):
+    """Hash of the kernel sources a profile was taken on: the listed files of
+    the package's csrc/ (all of them when none are listed)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_gemm_tcgen05_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    if files is None:
+        files = sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    for f in files:
+        path = os.path.join(csrc, f)
+        if not os.path.exists(path):
+            return None
+        with open(path, "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
-def profile_traffic(cfg):
+def profile_traffic(cfg, choice):
     """Per-launch DRAM bytes from the committed ncu summary of this workload,
-    or None when it is missing or was taken on other kernel sources."""
+    or None when it is missing, was taken on other kernel sources, or on
+    another kernel choice than the one this run dispatched."""
     import glob
     found = sorted(glob.glob(os.path.join(ROOT, "profiles", f"*_{cfg}.md")))
     if not found:
         return None
-    path = found[0]
-    text = open(path).read()
+    text = open(found[0]).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     s = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
-    if not m or not s or s.group(1) != kernel_source_hash():
+    f = re.search(r"kernel_sources:\s*(.+)", text)
+    files = f.group(1).split() if f else None
+    c = re.search(r"kernel_choice:\s*(\S+)", text)
+    if not m or not s or s.group(1) != kernel_source_hash(files):
+        return None
+    if c and c.group(1) != choice:
         return None
     return float(m.group(1))
 
@@ -375,7 +386,7 @@ def run_ours(args, rank, world, cfg):
         achieved = flops / avg_launch_s / 1e12
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
         r_unit = "TFLOP/s"
-    traffic = profile_traffic(cfg)
+    traffic = profile_traffic(cfg, choice)
     clocks = sampler.summary(t0, t1)
     line = {
         "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": args.steps,
