@@ -53,6 +53,9 @@ namespace {
 
 bool is16(int32_t t) { return t == GEMM_F16 || t == GEMM_BF16; }
 bool is_float_out(int32_t t) { return t == GEMM_F32 || t == GEMM_F16 || t == GEMM_BF16; }
+static_assert(GEMM_F32 == DT_F32 && GEMM_F16 == DT_F16 && GEMM_BF16 == DT_BF16 && GEMM_S4 == DT_S4,
+              "the C ABI's dtype codes are the kernels' codes");
+
 int64_t elem_bytes_x2(int32_t t) { return t == GEMM_F32 ? 8 : (t == GEMM_S4 ? 1 : 4); }  // 2 * bytes
 
 bool device_pointer_uncached(const void* p) {

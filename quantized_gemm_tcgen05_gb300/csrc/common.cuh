@@ -20,7 +20,7 @@ constexpr uint32_t EPI_SMEM_BYTES = 32 * 1024;
 constexpr int EPI_CBARS = 16;  // 4 epilogue warps x up to 4 buffers
 
 // TMEM is allocated in power-of-two column counts of at least 32.
-constexpr uint32_t tmem_cols_for(uint32_t cols) {
+__host__ __device__ constexpr uint32_t tmem_cols_for(uint32_t cols) {
     uint32_t n = 32;
     while (n < cols) n *= 2;
     return n;
