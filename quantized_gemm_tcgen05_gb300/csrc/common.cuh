@@ -284,13 +284,51 @@ __device__ __forceinline__ float4* partial_quad(float* partials, int64_t slot, i
     return reinterpret_cast<float4*>(partials + slot * (int64_t)(BM * BN)) + ((int64_t)(c * Q + j) * BM + r);
 }
 
+// Shared memory the last arriver of a split tile may use to reduce the
+// partials of its CTA's final unit: the pipeline ring, idle once the final
+// unit's accumulator is complete.  base == nullptr: not available.
+struct FixupSmem {
+    uint8_t* base;
+    uint32_t bytes;
+    uint64_t* bar;  // completion barrier of the bulk copies (used at most once)
+};
+
+// Whether unit `u` (just returned by the iterator `w`) is this program's last.
+__device__ __forceinline__ bool final_unit(const GemmKernelParams& P, WorkIter w, int bn) {
+    Unit u2;
+    return !next_unit(P, w, u2, bn);
+}
+
+// The last arriver of a split tile copies every contributor's partial tile
+// (BM x BN fp32, contiguous per slot) into the idle ring with bulk copies --
+// all in flight at once instead of a few loads per thread -- and waits for
+// them.  Called by all epilogue threads; returns false if the wait gave up.
+template <int BN>
+__device__ __forceinline__ bool fixup_bulk_load(const GemmKernelParams& P, const Unit& u, const FixupSmem& fx,
+                                                const Guard& g) {
+    constexpr uint32_t TILE_BYTES = BM * BN * 4;
+    if (threadIdx.x == 64) {
+        fence_proxy_async_global();  // the contributors' partial stores -> our bulk reads
+        mbar_arrive_expect_tx(fx.bar, (uint32_t)u.ncontrib * TILE_BYTES);
+        for (int q = 0; q < u.ncontrib; ++q)
+            bulk_load_g2s(fx.base + (size_t)q * TILE_BYTES,
+                          P.partials + partial_slot(P.sched, u.tile, q) * (int64_t)(BM * BN), TILE_BYTES, fx.bar);
+    }
+    return __all_sync(0xffffffffu, wait_bar(fx.bar, 0, g, SITE_EPI_TMEM_FULL));
+}
+
+template <int BN>
+__device__ __forceinline__ bool fixup_fits(const FixupSmem& fx, const Unit& u) {
+    return fx.base != nullptr && (uint64_t)u.ncontrib * BM * BN * 4 <= fx.bytes;
+}
+
 // The epilogue role: 4 warps (128 threads), warp w reads TMEM lanes
 // 32*(w%4) .. 32*(w%4)+31.  For every unit: wait for the accumulator, then
 // either store it (whole tile) or write it as a partial and, if this unit is
 // the last of its tile to arrive, reduce all partials in K order and store.
 template <int BN>
 __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uint64_t* tfull, uint64_t* tempty,
-                              float* staging_all, volatile uint32_t* bcast, const Guard& g) {
+                              float* staging_all, volatile uint32_t* bcast, const FixupSmem& fx, const Guard& g) {
     using CK = Chunk<BN>;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int ew = warp % 4;
@@ -346,6 +384,8 @@ __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uin
         epi_bar_sync();
         if (*bcast == 0u) continue;
         __threadfence();
+        const bool bulk = fixup_fits<BN>(fx, u) && final_unit(P, w, BN);
+        if (bulk && !fixup_bulk_load<BN>(P, u, fx, g)) break;
 #pragma unroll 1
         for (int c = 0; c < CK::N; ++c) {
             CChunk<CK::W> cc;
@@ -353,6 +393,23 @@ __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uin
             float v[CK::W];
 #pragma unroll
             for (int i = 0; i < CK::W; ++i) v[i] = 0.0f;
+            if (bulk) {
+                // contributors in K order, from the ring
+#pragma unroll 1
+                for (int q = 0; q < u.ncontrib; ++q) {
+                    const float4* src = reinterpret_cast<const float4*>(fx.base + (size_t)q * (BM * BN * 4));
+#pragma unroll
+                    for (int j = 0; j < CK::Q; ++j) {
+                        const float4 p = src[(c * CK::Q + j) * BM + r];
+                        v[4 * j] += p.x;
+                        v[4 * j + 1] += p.y;
+                        v[4 * j + 2] += p.z;
+                        v[4 * j + 3] += p.w;
+                    }
+                }
+                store_chunk<CK::W>(P.epi, u, ew, lane, c * CK::W, v, cc, staging);
+                continue;
+            }
             // contributors in K order, two at a time so their loads overlap
 #pragma unroll 1
             for (int q0 = 0; q0 < u.ncontrib; q0 += 2) {
@@ -417,7 +474,7 @@ struct ChunkStream {
 template <int BN>
 __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, const CUtensorMap* tmD,
                              uint32_t tmem_base, uint64_t* tfull, uint64_t* tempty, uint8_t* ebuf_all,
-                             uint64_t* cbar_all, volatile uint32_t* bcast, const Guard& g) {
+                             uint64_t* cbar_all, volatile uint32_t* bcast, const FixupSmem& fx, const Guard& g) {
     constexpr int W = 32;
     constexpr int NCH = BN / W;
     const EpiParams& e = P.epi;
@@ -435,7 +492,7 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
     auto slab_x = [&](const Unit& u, int c) { return (int32_t)(u.y_row0 + c * W); };
     auto slab_y = [&](const Unit& u) { return (int32_t)(u.x_row0 + ew * 32); };
 
-    // Store bookkeeping (lane 0): stores are numbered as they are committed;
+    // Store bookkeeping (all lanes; lane 0 issues): stores are numbered as they are committed;
     // a buffer may be rewritten once every store up to its last one has read
     // its source, i.e. once at most nstores - last_store[b] are still reading.
     uint32_t nstores = 0;
@@ -483,8 +540,11 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
                 ok = false;
                 return;
             }
-        } else {
-            if (lane == 0) wait_buffer_read(b);  // its previous store has read it
+        } else if (store && last_store[b] != 0) {
+            // the buffer's previous store must have read it; a buffer never
+            // stored from, or not written now, needs no wait (the bulk-group
+            // wait costs about a microsecond even with nothing pending)
+            if (lane == 0) wait_buffer_read(b);
             __syncwarp();
         }
         if (store) {
@@ -533,18 +593,24 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
             fence_proxy_async_smem();
         }
         __syncwarp();
-        if (store && lane == 0) {
-            if (P.x3d)
-                tma_store_3d(tmD, buf, slab_x(u, c), slab_y(u), u.batch);
-            else
-                tma_store_2d(tmD, buf, slab_x(u, c), slab_y(u));
-            bulk_commit_group();
+        if (store) {
+            if (lane == 0) {
+                if (P.x3d)
+                    tma_store_3d(tmD, buf, slab_x(u, c), slab_y(u), u.batch);
+                else
+                    tma_store_2d(tmD, buf, slab_x(u, c), slab_y(u));
+                bulk_commit_group();
+            }
+            // every lane keeps the count, so the waits below are taken (or
+            // skipped) by the whole warp
             last_store[b] = ++nstores;
         }
         ++gpos;
         if (use_c && pre.valid) {
-            if (lane == 0) wait_buffer_read(ppos % ncb);  // the next slab's buffer is free
-            __syncwarp();
+            if (last_store[ppos % ncb] != 0) {
+                if (lane == 0) wait_buffer_read(ppos % ncb);  // the next slab's buffer is free
+                __syncwarp();
+            }
             issue_c();
         }
     };
@@ -595,12 +661,28 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
         epi_bar_sync();
         const bool last = *bcast != 0u;
         if (last) __threadfence();
+        const bool bulk = last && fixup_fits<BN>(fx, u) && final_unit(P, w, BN);
+        if (bulk && !fixup_bulk_load<BN>(P, u, fx, g)) break;
 #pragma unroll 1
         for (int c = 0; c < NCH && ok; ++c) {
             float v[W];
 #pragma unroll
             for (int i = 0; i < W; ++i) v[i] = 0.0f;
-            if (last) {
+            if (bulk) {
+                // contributors in K order, from the ring
+#pragma unroll 1
+                for (int q = 0; q < u.ncontrib; ++q) {
+                    const float4* src = reinterpret_cast<const float4*>(fx.base + (size_t)q * (BM * BN * 4));
+#pragma unroll
+                    for (int j = 0; j < W / 4; ++j) {
+                        const float4 p = src[(c * (W / 4) + j) * BM + r];
+                        v[4 * j] += p.x;
+                        v[4 * j + 1] += p.y;
+                        v[4 * j + 2] += p.z;
+                        v[4 * j + 3] += p.w;
+                    }
+                }
+            } else if (last) {
 #pragma unroll 1
                 for (int q0 = 0; q0 < u.ncontrib; q0 += 2) {
                     const bool two = q0 + 1 < u.ncontrib;
@@ -644,14 +726,15 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
 template <int BN>
 __device__ __forceinline__ void epilogue(const GemmKernelParams& P, const CUtensorMap* tmC, const CUtensorMap* tmD,
                                          uint32_t tmem_base, uint64_t* tfull, uint64_t* tempty, uint8_t* esmem,
-                                         uint64_t* cbar, volatile uint32_t* bcast, const Guard& g) {
+                                         uint64_t* cbar, volatile uint32_t* bcast, const FixupSmem& fx,
+                                         const Guard& g) {
     if constexpr (BN >= 32) {
         if (P.epi.tma) {
-            epilogue_tma<BN>(P, tmC, tmD, tmem_base, tfull, tempty, esmem, cbar, bcast, g);
+            epilogue_tma<BN>(P, tmC, tmD, tmem_base, tfull, tempty, esmem, cbar, bcast, fx, g);
             return;
         }
     }
-    epilogue_role<BN>(P, tmem_base, tfull, tempty, reinterpret_cast<float*>(esmem), bcast, g);
+    epilogue_role<BN>(P, tmem_base, tfull, tempty, reinterpret_cast<float*>(esmem), bcast, fx, g);
 }
 
 }  // namespace qg

@@ -37,7 +37,7 @@ struct UmmaCfg {
     static constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * BN);
     static constexpr uint32_t STAGING_BYTES = EPI_SMEM_BYTES;
     static constexpr int MAX_STAGES = 16;
-    static constexpr uint32_t AUX_BYTES = (2 * MAX_STAGES + 5 + EPI_CBARS) * 8 + 16;
+    static constexpr uint32_t AUX_BYTES = (2 * MAX_STAGES + 6 + EPI_CBARS) * 8 + 16;
     static constexpr uint32_t FIXED_BYTES = 1024 /*alignment slack*/ + STAGING_BYTES + AUX_BYTES;
     static size_t smem_bytes(int stages) { return FIXED_BYTES + (size_t)stages * STAGE_BYTES; }
     static int max_stages() {
@@ -64,7 +64,8 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t* tempty = tfull + 2;
     uint64_t* done = tempty + 2;
     uint64_t* cbar = done + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cbar + EPI_CBARS);
+    uint64_t* fixbar = cbar + EPI_CBARS;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fixbar + 1);
     volatile uint32_t* bcast = tmem_slot + 1;
     volatile uint32_t* abort_flag = tmem_slot + 2;
 
@@ -80,6 +81,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         mbar_init(done, 1);
         for (int i = 0; i < EPI_CBARS; ++i) mbar_init(&cbar[i], 1);
+        mbar_init(fixbar, 1);
         *bcast = 0;
         *abort_flag = 0;
         fence_barrier_init();
@@ -180,7 +182,8 @@ __global__ void __launch_bounds__(192, 1)
             }
         }
     } else {
-        epilogue<BN>(P, &tmC, &tmD, tmem_base, tfull, tempty, reinterpret_cast<uint8_t*>(staging), cbar, bcast, g);
+        const FixupSmem fx{ring, (uint32_t)((size_t)S * Cfg::STAGE_BYTES), fixbar};
+        epilogue<BN>(P, &tmC, &tmD, tmem_base, tfull, tempty, reinterpret_cast<uint8_t*>(staging), cbar, bcast, fx, g);
     }
 
     tc_fence_before_sync();

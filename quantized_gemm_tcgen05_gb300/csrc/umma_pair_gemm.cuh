@@ -244,7 +244,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             }
         }
     } else {
-        epilogue<BN>(P, &tmC, &tmD, tmem_base, tfull, tempty, esmem, cbar, bcast, g);
+        const FixupSmem fx{nullptr, 0u, nullptr};  // data-parallel only: no partial tiles
+        epilogue<BN>(P, &tmC, &tmD, tmem_base, tfull, tempty, esmem, cbar, bcast, fx, g);
     }
 
     tc_fence_before_sync();
