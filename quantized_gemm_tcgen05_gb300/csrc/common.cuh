@@ -5,6 +5,10 @@
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <utility>
 
 #include "kparams.h"
 #include "ptx.cuh"
@@ -24,6 +28,36 @@ __host__ __device__ constexpr uint32_t tmem_cols_for(uint32_t cols) {
     uint32_t n = 32;
     while (n < cols) n *= 2;
     return n;
+}
+
+// ---- launches ------------------------------------------------------------------
+
+// Programmatic dependent launch is on unless GEMM_PDL=0: a GEMM kernel may
+// then be scheduled while the previous kernel in the stream finishes, doing
+// its set-up early; it waits for that kernel before touching memory.
+inline bool pdl_enabled() {
+    static const bool on = [] {
+        const char* e = getenv("GEMM_PDL");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // ---- bounded waits -------------------------------------------------------------

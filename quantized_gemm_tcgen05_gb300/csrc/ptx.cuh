@@ -149,6 +149,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---- programmatic dependent launch ------------------------------------------------------
+
+// Let the next kernel in the stream (launched with programmatic stream
+// serialization) be scheduled now; it still waits for this grid to finish
+// before it touches memory (griddep_wait).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the grids this one depends on have completed and their memory
+// operations are visible.  Returns at once when there are none.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- tcgen05 -------------------------------------------------------------------------
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {

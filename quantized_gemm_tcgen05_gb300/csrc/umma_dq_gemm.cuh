@@ -306,6 +306,10 @@ __global__ void __launch_bounds__(192 + XF_THREADS, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // set-up (barriers, TMEM, descriptor prefetch) overlaps the previous
+    // kernel's tail; no global memory is touched before the previous grid is done
+    griddep_launch_dependents();
+    griddep_wait();
     const Guard g{P.status, P.timeout_ns, abort_flag};
 
     auto x_op = [&](int s) { return ring + (size_t)s * Cfg::STAGE_BYTES; };
@@ -455,8 +459,7 @@ cudaError_t launch_dq_bn(const GemmMaps& m, const GemmKernelParams& p, int grid,
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
-    umma_dq_gemm_kernel<BN><<<grid, 192 + XF_THREADS, smem, st>>>(m.x, m.y, m.c, m.d, m.xs, m.ys, p);
-    return cudaGetLastError();
+    return launch_pdl(umma_dq_gemm_kernel<BN>, grid, 192 + XF_THREADS, smem, st, m.x, m.y, m.c, m.d, m.xs, m.ys, p);
 }
 
 template <int BN>

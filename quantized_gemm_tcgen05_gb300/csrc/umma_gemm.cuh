@@ -98,6 +98,10 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // set-up (barriers, TMEM, descriptor prefetch) overlaps the previous
+    // kernel's tail; no global memory is touched before the previous grid is done
+    griddep_launch_dependents();
+    griddep_wait();
     const Guard g{P.status, P.timeout_ns, abort_flag};
 
     if (warp == 0) {
@@ -210,8 +214,7 @@ cudaError_t launch_umma_bn(const GemmMaps& m, const GemmKernelParams& p, int gri
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
-    umma_gemm_kernel<BN><<<grid, 192, smem, st>>>(m.x, m.y, m.c, m.d, p);
-    return cudaGetLastError();
+    return launch_pdl(umma_gemm_kernel<BN>, grid, 192, smem, st, m.x, m.y, m.c, m.d, p);
 }
 
 template <int BN>

@@ -119,6 +119,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     cluster_sync();  // both CTAs' barriers exist before any cross-CTA arrive
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // set-up overlaps the previous kernel's tail; no global memory is
+    // touched before the previous grid is done
+    griddep_launch_dependents();
+    griddep_wait();
     const Guard g{P.status, P.timeout_ns, abort_flag};
 
     if (warp == 0) {
@@ -271,8 +275,8 @@ cudaError_t launch_pair_bn(const GemmMaps& m, const GemmKernelParams& p, int gri
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
-    umma_pair_gemm_kernel<BN><<<grid, 192, PairCfg<BN>::smem_bytes(p.stages), st>>>(m.x, m.y, m.c, m.d, p);
-    return cudaGetLastError();
+    return launch_pdl(umma_pair_gemm_kernel<BN>, grid, 192, PairCfg<BN>::smem_bytes(p.stages), st, m.x, m.y, m.c,
+                      m.d, p);
 }
 
 template <int BN>
