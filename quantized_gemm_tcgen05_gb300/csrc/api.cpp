@@ -205,6 +205,20 @@ int make_map(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t type, int6
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+// Tensor map over a 16-bit K-major operand viewed as [K/64 chunks][rows][64]:
+// a box of two 64-wide chunks x box_rows rows lands as two SWIZZLE_128B
+// tiles, one copy for two K-steps.  Only for K a multiple of 64 (the 64-wide
+// inner dimension must not run past a row).
+int make_map_kchunk(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t type, int64_t K, int64_t rows, int64_t ld,
+                    int32_t box_rows) {
+    CUtensorMapDataType dt = type == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(K / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)ld * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 2};
+    CUresult r = encode_cached(h, m, dt, 3, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
 // Tensor map over packed int4 rows: [rows][K/2 bytes], box 32 bytes x rows,
 // no swizzle (the dequantising warps rewrite the tile into the swizzled
 // layout the tensor core reads).
@@ -259,6 +273,16 @@ int capacity(gemm_handle* h, const Choice& c) {
     return cap < h->sm_count ? cap : h->sm_count;
 }
 
+// The CTA-pair kernel copies two K-steps per TMA box when K is a multiple of
+// 64 and the problem is not batched (GEMM_PAIR_KS=1 keeps one K-step).
+bool pair_kchunks(const Problem& p) {
+    static const bool allowed = [] {
+        const char* e = getenv("GEMM_PAIR_KS");
+        return !(e && e[0] == '1');
+    }();
+    return allowed && p.K % 64 == 0 && p.batches == 1 && p.K >= 64;
+}
+
 int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_workspace_t* ws, cudaStream_t st) {
     GemmKernelParams kp;
     memset(&kp, 0, sizeof kp);
@@ -310,6 +334,12 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
         rc = s4 ? make_map_s4(h, &tx, p.B, p.K, p.N, p.ldb, 128) : make_map(h, &tx, p.B, p.b_type, p.K, p.N, p.ldb, 1, 0, 128);
         if (rc == GEMM_OK) rc = make_map(h, &ty, p.A, p.a_type, p.K, p.M, p.lda, 1, 0, c.bn);
         kp.x3d = kp.y3d = 0;
+    } else if (c.pair && pair_kchunks(p)) {
+        // the CTA pair loads half of the Y tile in each CTA, two K-steps per copy
+        rc = make_map_kchunk(h, &tx, p.A, p.a_type, p.K, p.M, p.lda, 128);
+        if (rc == GEMM_OK) rc = make_map_kchunk(h, &ty, p.B, p.b_type, p.K, p.N, p.ldb, c.bn / 2);
+        kp.x3d = kp.y3d = 0;
+        kp.ks = 2;
     } else {
         rc = make_map(h, &tx, p.A, p.a_type, p.K, p.M, p.lda, p.batches, p.a_bs, 128);
         // the CTA pair loads half of the Y tile in each CTA
@@ -377,7 +407,8 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
         cudaError_t ce = launch_umma_dq_gemm(c.bn, maps, kp, kp.sched.programs, st);
         return ce == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
-    kp.stages = c.pair ? umma_pair_max_stages(c.bn) : umma_max_stages(c.bn);
+    if (kp.ks == 0) kp.ks = 1;
+    kp.stages = c.pair ? umma_pair_max_stages(c.bn, kp.ks) : umma_max_stages(c.bn);
     if (kp.stages < 2) return GEMM_ERR_NO_KERNEL;
     if (const char* fs = getenv("GEMM_STAGES")) {  // ring depth override for tuning sweeps
         const int want = atoi(fs);

@@ -67,10 +67,10 @@ cudaError_t launch_umma_pair_gemm(int bn, const GemmMaps& m, const GemmKernelPar
     }
 }
 
-int umma_pair_max_stages(int bn) {
+int umma_pair_max_stages(int bn, int ks) {
     switch (bn) {
 #define QG_CASE(B) \
-    case B: return pair_stages_bn<B>();
+    case B: return pair_stages_bn<B>(ks);
         QG_FOR_EACH_PAIR_BN(QG_CASE)
 #undef QG_CASE
         default: return 0;

@@ -42,9 +42,10 @@ struct PairCfg {
     static constexpr uint32_t EPI_BYTES = EPI_SMEM_BYTES / 2;
     static constexpr uint32_t AUX_BYTES = (2 * MAX_STAGES + 7 + EPI_CBARS) * 8 + 16;
     static constexpr uint32_t FIXED_BYTES = 1024 + EPI_BYTES + AUX_BYTES;
-    static size_t smem_bytes(int stages) { return FIXED_BYTES + (size_t)stages * STAGE_BYTES; }
-    static int max_stages() {
-        int s = (int)((232448 - FIXED_BYTES) / STAGE_BYTES);
+    // a stage holds ks 64-wide K-steps of both operands
+    static size_t smem_bytes(int stages, int ks) { return FIXED_BYTES + (size_t)stages * ks * STAGE_BYTES; }
+    static int max_stages(int ks) {
+        int s = (int)((232448 - FIXED_BYTES) / (ks * STAGE_BYTES));
         return s > MAX_STAGES ? MAX_STAGES : s;
     }
 };
@@ -74,8 +75,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = P.stages;
+    const int KS = P.ks;  // K-steps per stage: 1, or 2 with K-chunk tensor maps (one box per operand per stage)
+    const uint32_t stage_bytes = (uint32_t)KS * Cfg::STAGE_BYTES;
+    const uint32_t a_region = (uint32_t)KS * Cfg::A_BYTES;
     uint8_t* ring = smem;
-    uint8_t* esmem = smem + (size_t)S * Cfg::STAGE_BYTES;
+    uint8_t* esmem = smem + (size_t)S * stage_bytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(esmem + Cfg::EPI_BYTES);
     uint64_t* empty = full + Cfg::MAX_STAGES;
     uint64_t* tfull = empty + Cfg::MAX_STAGES;
@@ -137,14 +141,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             while (ok && next_unit(P, w, u, BN)) {
                 // this CTA's half of the Y tile
                 const int32_t y0 = (int32_t)(u.y_row0 + (int64_t)rank * Cfg::BH);
-                for (int k = u.k_begin; k < u.k_end; ++k) {
+                for (int k = u.k_begin; k < u.k_end; k += KS) {
                     if (!wait_bar(&empty[s], ph ^ 1, g, SITE_PRODUCER_EMPTY)) {
                         ok = false;
                         break;
                     }
-                    uint8_t* a = ring + (size_t)s * Cfg::STAGE_BYTES;
-                    uint8_t* b = a + Cfg::A_BYTES;
-                    if (leader) {
+                    uint8_t* a = ring + (size_t)s * stage_bytes;
+                    uint8_t* b = a + a_region;
+                    if (KS == 2) {
+                        // K-chunk maps: coordinates (0, row, chunk), boxes of two 64-wide chunks
+                        // (past the last chunk TMA fills zeros and still counts the bytes)
+                        if (leader) {
+                            mbar_arrive_expect_tx(&full[s], 2 * KS * (Cfg::A_BYTES + Cfg::B_BYTES));
+                            tma_load_3d(a, &tmX, &full[s], 0, (int32_t)u.x_row0, k);
+                            tma_load_3d(b, &tmY, &full[s], 0, y0, k);
+                        } else {
+                            const uint32_t lf = mapa_shared(smem_u32(&full[s]), 0);
+                            tma_load_3d_pair(a, &tmX, lf, 0, (int32_t)u.x_row0, k);
+                            tma_load_3d_pair(b, &tmY, lf, 0, y0, k);
+                        }
+                    } else if (leader) {
                         mbar_arrive_expect_tx(&full[s], 2 * (Cfg::A_BYTES + Cfg::B_BYTES));
                         if (P.x3d)
                             tma_load_3d(a, &tmX, &full[s], k * BK, (int32_t)u.x_row0, u.batch);
@@ -202,18 +218,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     break;
                 tc_fence_after_sync();
                 const uint32_t d = tmem_base + (uint32_t)(buf * BN);
-                for (int k = u.k_begin; k < u.k_end; ++k) {
+                for (int k = u.k_begin; k < u.k_end; k += KS) {
                     if (!wait_bar(&full[s], ph, g, SITE_MMA_FULL)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a_addr = smem_u32(ring + (size_t)s * Cfg::STAGE_BYTES);
-                    const uint64_t ad = make_sw128_kmajor_desc(a_addr);
-                    const uint64_t bd = make_sw128_kmajor_desc(a_addr + Cfg::A_BYTES);
+                    const uint32_t a_addr = smem_u32(ring + (size_t)s * stage_bytes);
+                    const int nk = u.k_end - k < KS ? u.k_end - k : KS;
+                    for (int h = 0; h < nk; ++h) {
+                        const uint64_t ad = make_sw128_kmajor_desc(a_addr + h * Cfg::A_BYTES);
+                        const uint64_t bd = make_sw128_kmajor_desc(a_addr + a_region + h * Cfg::B_BYTES);
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk)
-                        umma_f16_ss_pair(d, ad + 2 * kk, bd + 2 * kk, P.idesc, (k > u.k_begin || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                            umma_f16_ss_pair(d, ad + 2 * kk, bd + 2 * kk, P.idesc,
+                                             (k + h > u.k_begin || kk > 0) ? 1u : 0u);
+                    }
                     issued = true;
                     umma_commit_pair_mc(&empty[s], 0x3);
                     if (++s == S) {
@@ -270,24 +290,23 @@ cudaError_t launch_pair_bn(const GemmMaps& m, const GemmKernelParams& p, int gri
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(configured.load() & bit)) {
-        e = cudaFuncSetAttribute(umma_pair_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)PairCfg<BN>::smem_bytes(PairCfg<BN>::max_stages()));
+        e = cudaFuncSetAttribute(umma_pair_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
-    return launch_pdl(umma_pair_gemm_kernel<BN>, grid, 192, PairCfg<BN>::smem_bytes(p.stages), st, m.x, m.y, m.c,
-                      m.d, p);
+    return launch_pdl(umma_pair_gemm_kernel<BN>, grid, 192, PairCfg<BN>::smem_bytes(p.stages, p.ks), st, m.x, m.y,
+                      m.c, m.d, p);
 }
 
 template <int BN>
-int pair_stages_bn() {
-    return PairCfg<BN>::max_stages();
+int pair_stages_bn(int ks) {
+    return PairCfg<BN>::max_stages(ks);
 }
 
 // Clusters of two that can be resident at once with the largest ring.
 template <int BN>
 int pair_max_clusters_bn() {
-    const size_t smem = PairCfg<BN>::smem_bytes(PairCfg<BN>::max_stages());
+    const size_t smem = PairCfg<BN>::smem_bytes(PairCfg<BN>::max_stages(1), 1);
     if (cudaFuncSetAttribute(umma_pair_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess) {
         cudaGetLastError();

@@ -23,7 +23,10 @@ def lib():
 
 
 @pytest.mark.parametrize("bn", [128, 224, 256])
-@pytest.mark.parametrize("shape", [(256, 256, 128), (300, 520, 712), (1000, 777, 64 * 9 + 8), (129, 33, 72)])
+# K a multiple of 64 copies two K-steps per box (odd chunk counts end on a
+# half-filled stage); other K one K-step per box
+@pytest.mark.parametrize("shape", [(256, 256, 128), (300, 520, 712), (1000, 777, 64 * 9 + 8), (129, 33, 72),
+                                   (384, 448, 64 * 13), (512, 300, 4096)])
 def test_pair_kernel_parity(lib, bn, shape, monkeypatch):
     monkeypatch.setenv("GEMM_FORCE_KERNEL", f"umma2_bn{bn}/dp")
     M, N, K = shape
