@@ -288,8 +288,8 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
     memset(&kp, 0, sizeof kp);
     if (c.pair && capacity(h, c) < 2) return GEMM_ERR_NO_KERNEL;
     kp.sched = make_sched(p, c, capacity(h, c));
-    const size_t need_p = partials_bytes_needed(kp.sched, c.bn);
-    const size_t need_c = counters_bytes_needed(kp.sched);
+    const size_t need_p = partials_bytes_needed(kp.sched, c.bn, c.pair);
+    const size_t need_c = counters_bytes_needed(kp.sched, c.pair);
     if (need_p || need_c) {
         if (!ws || !ws->partials || !ws->barriers || ws->partials_size < need_p || ws->barriers_size < need_c)
             return GEMM_ERR_WORKSPACE;
@@ -426,7 +426,7 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
 
 bool workspace_fits(gemm_handle* h, const Problem& p, const Choice& c, const gemm_workspace_t* ws) {
     SchedParams s = make_sched(p, c, capacity(h, c));
-    const size_t need_p = partials_bytes_needed(s, c.bn), need_c = counters_bytes_needed(s);
+    const size_t need_p = partials_bytes_needed(s, c.bn, c.pair), need_c = counters_bytes_needed(s, c.pair);
     if (!need_p && !need_c) return true;
     return ws && ws->partials && ws->barriers && ws->partials_size >= need_p && ws->barriers_size >= need_c;
 }
@@ -484,7 +484,7 @@ bool forced_kernel(const Problem& p, Choice* out) {
         return false;
     if (p.family == FAM_DQ && (c.bn == 192 || c.bn == 224)) return false;
     if (c.swap && (p.family == FAM_GROUPED || p.batches != 1)) return false;
-    if (c.pair && (p.family != FAM_DENSE || c.swap || c.sched != SCHED_DP ||
+    if (c.pair && (p.family != FAM_DENSE || c.swap || c.sched == SCHED_SPLITK ||
                    !(c.bn == 128 || c.bn == 224 || c.bn == 256)))
         return false;
     if (p.family == FAM_GROUPED) c.sched = SCHED_DP;
@@ -549,7 +549,7 @@ int dispatch_and_run(gemm_handle* h, const gemm_op_t* op, Problem& p, const gemm
         }
     }
     if (!have) {
-        c = heuristic(p, h->sm_count);
+        c = heuristic(p, h->sm_count, ws && ws->partials ? ws->partials_size : 0);
         if (forced_split > 1) {
             c.sched = SCHED_SPLITK;
             c.splits = forced_split;

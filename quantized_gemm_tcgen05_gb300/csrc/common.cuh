@@ -327,6 +327,15 @@ struct FixupSmem {
     uint64_t* bar;  // completion barrier of the bulk copies (used at most once)
 };
 
+// The CTA pair splits every tile into two 128-row halves, one per CTA, each
+// with its own partial slots and arrival counter.
+__device__ __forceinline__ int64_t half_slot(const GemmKernelParams& P, int64_t slot) {
+    return P.pair ? 2 * slot + (blockIdx.x & 1) : slot;
+}
+__device__ __forceinline__ int32_t* tile_counter(const GemmKernelParams& P, int64_t tile) {
+    return &P.counters[P.pair ? 2 * tile + (blockIdx.x & 1) : tile];
+}
+
 // Whether unit `u` (just returned by the iterator `w`) is this program's last.
 __device__ __forceinline__ bool final_unit(const GemmKernelParams& P, WorkIter w, int bn) {
     Unit u2;
@@ -346,7 +355,8 @@ __device__ __forceinline__ bool fixup_bulk_load(const GemmKernelParams& P, const
         mbar_arrive_expect_tx(fx.bar, (uint32_t)u.ncontrib * TILE_BYTES);
         for (int q = 0; q < u.ncontrib; ++q)
             bulk_load_g2s(fx.base + (size_t)q * TILE_BYTES,
-                          P.partials + partial_slot(P.sched, u.tile, q) * (int64_t)(BM * BN), TILE_BYTES, fx.bar);
+                          P.partials + half_slot(P, partial_slot(P.sched, u.tile, q)) * (int64_t)(BM * BN), TILE_BYTES,
+                          fx.bar);
     }
     return __all_sync(0xffffffffu, wait_bar(fx.bar, 0, g, SITE_EPI_TMEM_FULL));
 }
@@ -402,7 +412,7 @@ __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uin
             tmem_load_chunk<CK::W>(tbase + c * CK::W, v);
 #pragma unroll
             for (int j = 0; j < CK::Q; ++j)
-                *partial_quad<BN>(P.partials, u.slot, c, j, r) =
+                *partial_quad<BN>(P.partials, half_slot(P, u.slot), c, j, r) =
                     make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         }
         tc_fence_before_sync();
@@ -410,9 +420,9 @@ __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uin
         __threadfence();
         epi_bar_sync();
         if (threadIdx.x == 64) {
-            const int old = atomicAdd(&P.counters[u.tile], 1);
+            const int old = atomicAdd(tile_counter(P, u.tile), 1);
             const bool last = (old == u.ncontrib - 1);
-            if (last) atomicExch(&P.counters[u.tile], 0);  // every contributor has arrived
+            if (last) atomicExch(tile_counter(P, u.tile), 0);  // every contributor has arrived
             *bcast = last ? 1u : 0u;
         }
         epi_bar_sync();
@@ -448,8 +458,8 @@ __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uin
 #pragma unroll 1
             for (int q0 = 0; q0 < u.ncontrib; q0 += 2) {
                 const bool two = q0 + 1 < u.ncontrib;
-                const int64_t s0 = partial_slot(P.sched, u.tile, q0);
-                const int64_t s1 = two ? partial_slot(P.sched, u.tile, q0 + 1) : s0;
+                const int64_t s0 = half_slot(P, partial_slot(P.sched, u.tile, q0));
+                const int64_t s1 = two ? half_slot(P, partial_slot(P.sched, u.tile, q0 + 1)) : s0;
                 float4 p0[CK::Q], p1[CK::Q];
 #pragma unroll
                 for (int j = 0; j < CK::Q; ++j) {
@@ -679,7 +689,7 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
             tmem_load_chunk<W>(tbase + c * W, v);
 #pragma unroll
             for (int j = 0; j < W / 4; ++j)
-                *partial_quad<BN>(P.partials, u.slot, c, j, r) =
+                *partial_quad<BN>(P.partials, half_slot(P, u.slot), c, j, r) =
                     make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         }
         tc_fence_before_sync();
@@ -687,9 +697,9 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
         __threadfence();
         epi_bar_sync();
         if (threadIdx.x == 64) {
-            const int old = atomicAdd(&P.counters[u.tile], 1);
+            const int old = atomicAdd(tile_counter(P, u.tile), 1);
             const bool last = (old == u.ncontrib - 1);
-            if (last) atomicExch(&P.counters[u.tile], 0);
+            if (last) atomicExch(tile_counter(P, u.tile), 0);
             *bcast = last ? 1u : 0u;
         }
         epi_bar_sync();
@@ -720,8 +730,8 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
 #pragma unroll 1
                 for (int q0 = 0; q0 < u.ncontrib; q0 += 2) {
                     const bool two = q0 + 1 < u.ncontrib;
-                    const int64_t s0 = partial_slot(P.sched, u.tile, q0);
-                    const int64_t s1 = two ? partial_slot(P.sched, u.tile, q0 + 1) : s0;
+                    const int64_t s0 = half_slot(P, partial_slot(P.sched, u.tile, q0));
+                    const int64_t s1 = two ? half_slot(P, partial_slot(P.sched, u.tile, q0 + 1)) : s0;
                     float4 p0[W / 4], p1[W / 4];
 #pragma unroll
                     for (int j = 0; j < W / 4; ++j) {

@@ -89,6 +89,7 @@ SchedParams make_sched(const Problem& p, const Choice& c, int sm_count) {
         s.sk_full = (int32_t)pl.full_tiles;
         s.sk_partial = (int32_t)pl.partial_tiles;
         s.sk_factor = (int32_t)pl.sm_partition_factor;
+        s.sk_maxc = streamk_max_contrib(s.k_iters, s.sk_full);
     } else {
         s.kind = SCHED_DP;
         s.programs = (int32_t)(T < sm_count ? T : sm_count);
@@ -97,13 +98,14 @@ SchedParams make_sched(const Problem& p, const Choice& c, int sm_count) {
     return s;
 }
 
-size_t partials_bytes_needed(const SchedParams& s, int bn) {
-    return (size_t)partial_slots_needed(s) * 128 * (size_t)bn * sizeof(float);
+// The CTA pair keeps one partial slot and one counter per 128-row half tile.
+size_t partials_bytes_needed(const SchedParams& s, int bn, int pair) {
+    return (size_t)partial_slots_needed(s) * (pair ? 2 : 1) * 128 * (size_t)bn * sizeof(float);
 }
 
-size_t counters_bytes_needed(const SchedParams& s) {
+size_t counters_bytes_needed(const SchedParams& s, int pair) {
     if (s.kind == SCHED_DP) return 0;
-    return (size_t)total_tiles(s) * sizeof(int32_t);
+    return (size_t)total_tiles(s) * (pair ? 2 : 1) * sizeof(int32_t);
 }
 
 static int32_t swap_bn(int64_t M) {
@@ -155,17 +157,18 @@ std::vector<Choice> candidates(const Problem& p, int sm_count) {
         for (int32_t bn : {192, 224, 256}) add_scheds(bn, 0);
     if (swap_allowed(p)) add_scheds(swap_bn(p.M), 1);
     if (p.family == FAM_DENSE && p.M > 128)
-        for (int32_t bn : {128, 224, 256}) {
-            Choice c;
-            c.bn = bn;
-            c.pair = 1;
-            c.sched = SCHED_DP;
-            out.push_back(c);
-        }
+        for (int32_t bn : {128, 224, 256})
+            for (int32_t sched : {SCHED_DP, SCHED_STREAMK}) {
+                Choice c;
+                c.bn = bn;
+                c.pair = 1;
+                c.sched = sched;
+                out.push_back(c);
+            }
     return out;
 }
 
-Choice heuristic(const Problem& p, int sm_count) {
+Choice heuristic(const Problem& p, int sm_count, size_t partials_bytes) {
     // Measured on GB300 (152 SMs): full-width 128 x 256 tiles win whenever
     // there are at least as many tiles as SMs; below that, K is split so all
     // SMs stream -- into as many equal slices as fill one wave (split-K),
@@ -179,12 +182,13 @@ Choice heuristic(const Problem& p, int sm_count) {
     } else if (p.family == FAM_GROUPED) {
         c.bn = 256;  // measured best for ragged MoE blocks (the tile count is only an upper bound)
     } else {
-        // the tile width that minimises waves x width (time per wave grows
-        // with the width); wider wins ties.  256-row tiles on CTA pairs (half
-        // the Y-operand bytes per SM) whenever they fill at least one wave of
-        // clusters: a wave of pairs covers as many rows as a wave of single
-        // CTAs and measured about 20% faster.
-        int64_t best = -1;
+        // the tile shape that minimises waves x time per wave.  Per-wave
+        // times measured on GB300 at K = 4096 (64-wide K-steps, two per copy
+        // on pairs): CTA pair 15.6 + 0.032*bn us for 256 x bn tiles; single
+        // CTA 13.3 + 0.054*bn us for 128 x bn tiles.  Pairs need a full wave
+        // of clusters.
+        double best = -1.0;
+        int32_t best_sched = SCHED_DP;
         for (int32_t pair : {1, 0}) {
             if (pair && (p.family != FAM_DENSE || p.M <= 128)) continue;
             const int64_t cap = pair ? sm_count / 2 : sm_count;
@@ -195,13 +199,34 @@ Choice heuristic(const Problem& p, int sm_count) {
                 t.pair = pair;
                 const int64_t T = total_tiles(make_sched(p, t, sm_count));
                 if (pair && T < cap) continue;
-                const int64_t cost = ceil_div(T, cap) * bn * (pair ? 8 : 10);
-                if (best < 0 || cost < best) {
+                const double wave = pair ? 15.6 + 0.032 * bn : 13.3 + 0.054 * bn;
+                const double cost = (double)ceil_div(T, cap) * wave;
+                if (best < 0 || cost < best - 1e-9) {
                     best = cost;
                     c.bn = bn;
                     c.pair = pair;
+                    best_sched = SCHED_DP;
+                }
+                // stream-K over the pairs evens out a ragged last wave, at the
+                // price of partial tiles (measured: about half a wave for the
+                // plan's stream-K tiles), where the caller's workspace holds
+                // the partials
+                if (pair) {
+                    t.sched = SCHED_STREAMK;
+                    const SchedParams sk = make_sched(p, t, sm_count);
+                    const double sk_cost = ((double)T / cap + 0.5) * wave;
+                    if (partials_bytes_needed(sk, bn, 1) <= partials_bytes && sk_cost < best - 1e-9) {
+                        best = sk_cost;
+                        c.bn = bn;
+                        c.pair = 1;
+                        best_sched = SCHED_STREAMK;
+                    }
                 }
             }
+        }
+        if (c.pair) {  // pairs run data-parallel or stream-K (never split-K)
+            c.sched = best_sched;
+            return c;
         }
     }
     c.sched = SCHED_DP;
@@ -273,7 +298,7 @@ static bool valid_choice(const Key& k, const Choice& c) {
     if (!bn_ok || (c.swap != 0 && c.swap != 1) || c.sched < SCHED_DP || c.sched > SCHED_STREAMK) return false;
     if (c.splits < 1 || c.splits > 64 || !(c.us >= 0.0f)) return false;
     if (c.pair != 0 && c.pair != 1) return false;
-    if (c.pair && (c.swap || c.sched != SCHED_DP || k.family != FAM_DENSE)) return false;
+    if (c.pair && (c.swap || c.sched == SCHED_SPLITK || k.family != FAM_DENSE)) return false;
     if (c.pair && c.bn != 128 && c.bn != 224 && c.bn != 256) return false;
     if (k.family < FAM_DENSE || k.family > FAM_GROUPED) return false;
     if (k.N < 0 || k.K < 0 || k.m_bucket < 1 || k.batches < 1) return false;

@@ -61,13 +61,13 @@ Key make_key(const Problem& p);
 // Tiles of a problem under a choice, and the schedule parameters.
 // sm_count: SMs of the device; the CTA-pair kernel runs on clusters of two.
 SchedParams make_sched(const Problem& p, const Choice& c, int sm_count);
-size_t partials_bytes_needed(const SchedParams& s, int bn);
-size_t counters_bytes_needed(const SchedParams& s);
+size_t partials_bytes_needed(const SchedParams& s, int bn, int pair);
+size_t counters_bytes_needed(const SchedParams& s, int pair);
 
 // Every kernel variant that can run the problem.
 std::vector<Choice> candidates(const Problem& p, int sm_count);
 // The choice made without measuring.
-Choice heuristic(const Problem& p, int sm_count);
+Choice heuristic(const Problem& p, int sm_count, size_t partials_bytes);
 std::string choice_name(const Problem& p, const Choice& c);
 
 // Cache text format (see dispatch.cpp).

@@ -89,6 +89,7 @@ struct SchedParams {
     int32_t programs;   // persistent grid size
     // stream-K plan (SCHED_STREAMK)
     int32_t sk_tiles, sk_full, sk_partial, sk_factor;
+    int32_t sk_maxc;    // most programs one stream-K tile can have (partial slots per tile)
     // grouped GEMM: device offsets [E+1]; tiles_x is an upper bound then
     const int32_t* expert_offsets;
     int32_t num_experts;
@@ -130,17 +131,29 @@ QG_HD int64_t streamk_start(const SchedParams& s, int64_t pid) {
 // Split-K: tile * splits + idx.  Stream-K: each program owns two slots, the
 // first for the tile its range starts in and the second for the tile it ends
 // in.
+// Partial slot of contributor idx (in K order) of a split tile.  Stream-K
+// partial units only occur in the plan's stream-K tiles (the first sk_tiles),
+// each with at most sk_maxc contributors.
 QG_HD int64_t partial_slot(const SchedParams& s, int64_t tile, int32_t idx) {
     if (s.kind == SCHED_SPLITK) return tile * s.splits + idx;
-    int64_t q = streamk_owner(s, tile * s.k_iters) + idx;
-    int64_t first_tile = streamk_start(s, q) / s.k_iters;
-    return 2 * q + (first_tile == tile ? 0 : 1);
+    return tile * s.sk_maxc + idx;
 }
 
 QG_HD int64_t partial_slots_needed(const SchedParams& s) {
     if (s.kind == SCHED_SPLITK && s.splits > 1) return total_tiles(s) * s.splits;
-    if (s.kind == SCHED_STREAMK) return 2 * (int64_t)s.programs;
+    if (s.kind == SCHED_STREAMK) {
+        // programs of equal, whole-tile iteration ranges leave no partial tile
+        if (s.sk_partial == 0 && s.k_iters > 0 && s.sk_full % s.k_iters == 0) return 0;
+        return (int64_t)s.sk_tiles * s.sk_maxc;
+    }
     return 0;
+}
+
+// Contributors a stream-K tile can have: its k_iters iterations meet at most
+// ceil(k_iters / fewest iterations of a program) + 1 programs.
+QG_HD int32_t streamk_max_contrib(int32_t k_iters, int32_t sk_full) {
+    if (sk_full < 1) return 1;
+    return (k_iters + sk_full - 1) / sk_full + 1;
 }
 
 // Fill the coordinates of tile `t`.
@@ -235,10 +248,9 @@ struct WorkIter {
                     out.ncontrib = 1;
                 } else {
                     out.mode = UNIT_PARTIAL;
-                    bool first = (it == streamk_start(s, pid));
-                    out.slot = (int32_t)(2 * pid + (first ? 0 : 1));
                     int64_t q0 = streamk_owner(s, t * ipt);
                     int64_t q1 = streamk_owner(s, (t + 1) * ipt - 1);
+                    out.slot = (int32_t)partial_slot(s, t, (int32_t)(pid - q0));
                     out.ncontrib = (int32_t)(q1 - q0 + 1);
                 }
                 it = end;

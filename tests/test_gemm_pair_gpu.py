@@ -40,6 +40,27 @@ def test_pair_kernel_parity(lib, bn, shape, monkeypatch):
     assert qg.gemm_device_status(lib.h, qg.current_stream()) == 0
 
 
+@pytest.mark.parametrize("bn", [224, 256])
+@pytest.mark.parametrize("shape", [(1024, 1500, 4096), (600, 900, 64 * 21), (2048, 700, 1000)])
+def test_pair_kernel_streamk(lib, bn, shape, monkeypatch):
+    # stream-K over CTA pairs: each CTA keeps its own partial slots and
+    # arrival counter for its 128-row half of a split tile
+    monkeypatch.setenv("GEMM_FORCE_KERNEL", f"umma2_bn{bn}/streamk")
+    M, N, K = shape
+    p = synth.dense(M, N, K, seed=M + N + K + bn + 1, a_type=synth.BF16, d_type=synth.BF16, alpha=0.75, beta=-0.5,
+                    dist="normal", scale=0.1)
+    rc, D = run_problem(lib, p)
+    assert rc == 0, qg.gemm_status_string(rc)
+    assert qg.gemm_last_choice(lib.h) == f"umma2_bn{bn}/streamk"
+    ii, jj = sample_indices(M, N, 4000, seed=bn)
+    ref, bound = oracle.gemm_entries(p, ii, jj)
+    assert_close(D.double().cpu().numpy()[ii, jj], ref, bound, p.d_type, f"pair stream-K bn{bn} {shape}")
+    assert int(lib.ws.barriers.view(torch.int32).abs().sum().item()) == 0, "arrival counters left set"
+    rc, D2 = run_problem(lib, p)
+    assert rc == 0 and torch.equal(D, D2), "pair stream-K is not run-to-run deterministic"
+    assert qg.gemm_device_status(lib.h, qg.current_stream()) == 0
+
+
 def test_pair_kernel_one_hot_layout(lib, monkeypatch):
     # rows of both CTAs and both halves of the Y tile land where they belong
     monkeypatch.setenv("GEMM_FORCE_KERNEL", "umma2_bn256/dp")
