@@ -210,11 +210,11 @@ int make_map(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t type, int6
 // tiles, one copy for two K-steps.  Only for K a multiple of 64 (the 64-wide
 // inner dimension must not run past a row).
 int make_map_kchunk(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t type, int64_t K, int64_t rows, int64_t ld,
-                    int32_t box_rows) {
+                    int32_t box_rows, int32_t chunks) {
     CUtensorMapDataType dt = type == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(K / 64)};
     cuuint64_t strides[2] = {(cuuint64_t)ld * 2, 128};
-    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)chunks};
     CUresult r = encode_cached(h, m, dt, 3, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -273,14 +273,17 @@ int capacity(gemm_handle* h, const Choice& c) {
     return cap < h->sm_count ? cap : h->sm_count;
 }
 
-// The CTA-pair kernel copies two K-steps per TMA box when K is a multiple of
-// 64 and the problem is not batched (GEMM_PAIR_KS=1 keeps one K-step).
-bool pair_kchunks(const Problem& p) {
-    static const bool allowed = [] {
+// K-steps the CTA-pair kernel copies per TMA box: two when K is a multiple of
+// 64 and the problem is not batched, else one (GEMM_PAIR_KS=1|2|3 overrides
+// the two).
+int pair_kchunks(const Problem& p) {
+    static const int want = [] {
         const char* e = getenv("GEMM_PAIR_KS");
-        return !(e && e[0] == '1');
+        const int v = e ? atoi(e) : 2;
+        return v >= 1 && v <= 3 ? v : 2;
     }();
-    return allowed && p.K % 64 == 0 && p.batches == 1 && p.K >= 64;
+    if (want < 2 || p.K % 64 != 0 || p.batches != 1 || p.K < 64) return 1;
+    return want;
 }
 
 int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_workspace_t* ws, cudaStream_t st) {
@@ -334,12 +337,13 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
         rc = s4 ? make_map_s4(h, &tx, p.B, p.K, p.N, p.ldb, 128) : make_map(h, &tx, p.B, p.b_type, p.K, p.N, p.ldb, 1, 0, 128);
         if (rc == GEMM_OK) rc = make_map(h, &ty, p.A, p.a_type, p.K, p.M, p.lda, 1, 0, c.bn);
         kp.x3d = kp.y3d = 0;
-    } else if (c.pair && pair_kchunks(p)) {
-        // the CTA pair loads half of the Y tile in each CTA, two K-steps per copy
-        rc = make_map_kchunk(h, &tx, p.A, p.a_type, p.K, p.M, p.lda, 128);
-        if (rc == GEMM_OK) rc = make_map_kchunk(h, &ty, p.B, p.b_type, p.K, p.N, p.ldb, c.bn / 2);
+    } else if (c.pair && pair_kchunks(p) > 1) {
+        // the CTA pair loads half of the Y tile in each CTA, several K-steps per copy
+        const int ks = pair_kchunks(p);
+        rc = make_map_kchunk(h, &tx, p.A, p.a_type, p.K, p.M, p.lda, 128, ks);
+        if (rc == GEMM_OK) rc = make_map_kchunk(h, &ty, p.B, p.b_type, p.K, p.N, p.ldb, c.bn / 2, ks);
         kp.x3d = kp.y3d = 0;
-        kp.ks = 2;
+        kp.ks = ks;
     } else {
         rc = make_map(h, &tx, p.A, p.a_type, p.K, p.M, p.lda, p.batches, p.a_bs, 128);
         // the CTA pair loads half of the Y tile in each CTA

@@ -73,7 +73,7 @@ struct GemmKernelParams {
     uint32_t* status;     // device status words [4]
     uint64_t timeout_ns;  // bound on every wait
     int32_t pair;         // CTA-pair kernel: units are 256-row tiles shared by the two CTAs of a cluster
-    int32_t ks;           // CTA-pair kernel: 64-wide K-steps per stage (2: X/Y maps index 64-wide K chunks)
+    int32_t ks;           // CTA-pair kernel: 64-wide K-steps per stage (>1: X/Y maps index 64-wide K chunks)
 };
 
 // Instruction descriptor of tcgen05.mma.kind::f16: fp32 accumulator (bits

@@ -75,7 +75,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = P.stages;
-    const int KS = P.ks;  // K-steps per stage: 1, or 2 with K-chunk tensor maps (one box per operand per stage)
+    const int KS = P.ks;  // K-steps per stage: 1, or 2-3 with K-chunk tensor maps (one box per operand per stage)
     const uint32_t stage_bytes = (uint32_t)KS * Cfg::STAGE_BYTES;
     const uint32_t a_region = (uint32_t)KS * Cfg::A_BYTES;
     uint8_t* ring = smem;
@@ -150,8 +150,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     }
                     uint8_t* a = ring + (size_t)s * stage_bytes;
                     uint8_t* b = a + a_region;
-                    if (KS == 2) {
-                        // K-chunk maps: coordinates (0, row, chunk), boxes of two 64-wide chunks
+                    if (KS > 1) {
+                        // K-chunk maps: coordinates (0, row, chunk), boxes of KS 64-wide chunks
                         // (past the last chunk TMA fills zeros and still counts the bytes)
                         if (leader) {
                             mbar_arrive_expect_tx(&full[s], 2 * KS * (Cfg::A_BYTES + Cfg::B_BYTES));
