@@ -219,6 +219,18 @@ int make_map_kchunk(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t typ
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+// The same K-chunk view over a [batches][rows][K] operand (grouped experts):
+// [batches][K/64][rows][64], one expert per box.
+int make_map_kchunk4(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t type, int64_t K, int64_t rows,
+                     int64_t ld, int32_t batches, int64_t bstride, int32_t box_rows, int32_t chunks) {
+    CUtensorMapDataType dt = type == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)(K / 64), (cuuint64_t)batches};
+    cuuint64_t strides[3] = {(cuuint64_t)ld * 2, 128, (cuuint64_t)bstride * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)box_rows, (cuuint32_t)chunks, 1};
+    CUresult r = encode_cached(h, m, dt, 4, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
 // Tensor map over packed int4 rows: [rows][K/2 bytes], box 32 bytes x rows,
 // no swizzle (the dequantising warps rewrite the tile into the swizzled
 // layout the tensor core reads).
@@ -328,9 +340,20 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
     int rc;
     const bool dq = p.family == FAM_DQ;
     const bool s4 = p.b_type == GEMM_S4;
-    if (p.family == FAM_GROUPED) {
+    if (p.family == FAM_GROUPED && c.pair && pair_kchunks(p) > 1) {
+        // 256-row expert blocks on CTA pairs: each CTA its 128 token rows and
+        // half of the expert's Y tile, several K-steps per copy
+        const int ks = pair_kchunks(p);
+        rc = make_map_kchunk(h, &tx, p.A, p.a_type, p.K, p.M, p.lda, 128, ks);
+        if (rc == GEMM_OK)
+            rc = make_map_kchunk4(h, &ty, p.B, p.b_type, p.K, p.N, p.ldb, p.num_experts, p.b_bs, c.bn / 2, ks);
+        kp.x3d = 0;
+        kp.y3d = 1;
+        kp.ks = ks;
+    } else if (p.family == FAM_GROUPED) {
         rc = make_map(h, &tx, p.A, p.a_type, p.K, p.M, p.lda, 1, 0, 128);
-        if (rc == GEMM_OK) rc = make_map(h, &ty, p.B, p.b_type, p.K, p.N, p.ldb, p.num_experts, p.b_bs, c.bn);
+        if (rc == GEMM_OK)
+            rc = make_map(h, &ty, p.B, p.b_type, p.K, p.N, p.ldb, p.num_experts, p.b_bs, c.pair ? c.bn / 2 : c.bn);
         kp.x3d = 0;
         kp.y3d = 1;
     } else if (c.swap) {
@@ -488,7 +511,7 @@ bool forced_kernel(const Problem& p, Choice* out) {
         return false;
     if (p.family == FAM_DQ && (c.bn == 192 || c.bn == 224)) return false;
     if (c.swap && (p.family == FAM_GROUPED || p.batches != 1)) return false;
-    if (c.pair && (p.family != FAM_DENSE || c.swap || c.sched == SCHED_SPLITK ||
+    if (c.pair && ((p.family != FAM_DENSE && p.family != FAM_GROUPED) || c.swap || c.sched == SCHED_SPLITK ||
                    !(c.bn == 128 || c.bn == 224 || c.bn == 256)))
         return false;
     if (p.family == FAM_GROUPED) c.sched = SCHED_DP;

@@ -124,8 +124,12 @@ __device__ __forceinline__ int unit_pid(const GemmKernelParams& P) {
 __device__ __forceinline__ bool next_unit(const GemmKernelParams& P, WorkIter& w, Unit& u, int bn) {
     if (!P.pair) return w.next(P.sched, (int)blockIdx.x, BM, bn, u);
     if (!w.next(P.sched, (int)(blockIdx.x >> 1), 2 * BM, bn, u)) return false;
-    u.x_row0 += (int64_t)(blockIdx.x & 1) * BM;
-    u.x_rows = BM;
+    const int32_t half = (int32_t)(blockIdx.x & 1);
+    u.x_row0 += (int64_t)half * BM;
+    // a grouped 256-row block may hold fewer rows of its expert: each CTA
+    // keeps its share (possibly none; the epilogue then stores nothing)
+    const int32_t rows = P.sched.grouped ? u.x_rows - half * BM : BM;
+    u.x_rows = rows < 0 ? 0 : (rows > BM ? BM : rows);
     return true;
 }
 

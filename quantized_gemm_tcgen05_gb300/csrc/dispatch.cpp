@@ -51,8 +51,9 @@ SchedParams make_sched(const Problem& p, const Choice& c, int sm_count) {
     s.k_iters = (int32_t)ceil_div(p.K, BK_HOST);
     s.batches = p.batches;
     if (p.family == FAM_GROUPED) {
-        // upper bound on padded M-blocks: sum_e ceil(m_e / 128) <= T / 128 + E
-        s.tiles_x = (int32_t)(p.M / 128 + p.num_experts);
+        // upper bound on padded M-blocks: sum_e ceil(m_e / bm) <= T / bm + E
+        // (bm = 256 rows on CTA pairs)
+        s.tiles_x = (int32_t)(p.M / (c.pair ? 256 : 128) + p.num_experts);
         s.tiles_y = (int32_t)ceil_div(p.N, c.bn);
         s.batches = 1;
         s.grouped = 1;
@@ -165,6 +166,13 @@ std::vector<Choice> candidates(const Problem& p, int sm_count) {
                 c.sched = sched;
                 out.push_back(c);
             }
+    if (p.family == FAM_GROUPED && p.M > 128)
+        for (int32_t bn : {224, 256}) {
+            Choice c;
+            c.bn = bn;
+            c.pair = 1;
+            out.push_back(c);
+        }
     return out;
 }
 
@@ -180,7 +188,13 @@ Choice heuristic(const Problem& p, int sm_count, size_t partials_bytes) {
     } else if (p.family == FAM_DQ || p.N <= 128) {
         c.bn = 128;
     } else if (p.family == FAM_GROUPED) {
-        c.bn = 256;  // measured best for ragged MoE blocks (the tile count is only an upper bound)
+        // 256-row expert blocks on CTA pairs once they fill a wave of clusters
+        // (the tile count is an upper bound; blocks past an expert's rows are
+        // skipped), else single-CTA 128 x 256 tiles
+        c.bn = 256;
+        Choice t = c;
+        t.pair = 1;
+        if (p.M > 128 && total_tiles(make_sched(p, t, sm_count)) >= sm_count / 2) c.pair = 1;
     } else {
         // the tile shape that minimises waves x time per wave.  Per-wave
         // times measured on GB300 at K = 4096 (64-wide K-steps, two per copy
@@ -247,8 +261,9 @@ Choice heuristic(const Problem& p, int sm_count, size_t partials_bytes) {
 
 std::string choice_name(const Problem& p, const Choice& c) {
     char buf[96];
-    const char* fam =
-        p.family == FAM_DQ ? "umma_dq" : (p.family == FAM_GROUPED ? "umma_grouped" : (c.pair ? "umma2" : "umma"));
+    const char* fam = p.family == FAM_DQ
+                          ? "umma_dq"
+                          : (p.family == FAM_GROUPED ? (c.pair ? "umma2_grouped" : "umma_grouped") : (c.pair ? "umma2" : "umma"));
     const char* sk = c.sched == SCHED_DP ? "dp" : (c.sched == SCHED_STREAMK ? "streamk" : "splitk");
     if (c.sched == SCHED_SPLITK)
         snprintf(buf, sizeof buf, "%s_bn%d%s/%s%d", fam, c.bn, c.swap ? "_swap" : "", sk, c.splits);
@@ -298,7 +313,7 @@ static bool valid_choice(const Key& k, const Choice& c) {
     if (!bn_ok || (c.swap != 0 && c.swap != 1) || c.sched < SCHED_DP || c.sched > SCHED_STREAMK) return false;
     if (c.splits < 1 || c.splits > 64 || !(c.us >= 0.0f)) return false;
     if (c.pair != 0 && c.pair != 1) return false;
-    if (c.pair && (c.swap || c.sched == SCHED_SPLITK || k.family != FAM_DENSE)) return false;
+    if (c.pair && (c.swap || c.sched == SCHED_SPLITK || (k.family != FAM_DENSE && k.family != FAM_GROUPED))) return false;
     if (c.pair && c.bn != 128 && c.bn != 224 && c.bn != 256) return false;
     if (k.family < FAM_DENSE || k.family > FAM_GROUPED) return false;
     if (k.N < 0 || k.K < 0 || k.m_bucket < 1 || k.batches < 1) return false;

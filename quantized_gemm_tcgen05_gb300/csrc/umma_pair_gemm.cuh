@@ -153,14 +153,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     if (KS > 1) {
                         // K-chunk maps: coordinates (0, row, chunk), boxes of KS 64-wide chunks
                         // (past the last chunk TMA fills zeros and still counts the bytes)
+                        // (a batched / grouped Y operand adds the batch or expert coordinate)
                         if (leader) {
                             mbar_arrive_expect_tx(&full[s], 2 * KS * (Cfg::A_BYTES + Cfg::B_BYTES));
                             tma_load_3d(a, &tmX, &full[s], 0, (int32_t)u.x_row0, k);
-                            tma_load_3d(b, &tmY, &full[s], 0, y0, k);
+                            if (P.y3d)
+                                tma_load_4d(b, &tmY, &full[s], 0, y0, k, u.batch);
+                            else
+                                tma_load_3d(b, &tmY, &full[s], 0, y0, k);
                         } else {
                             const uint32_t lf = mapa_shared(smem_u32(&full[s]), 0);
                             tma_load_3d_pair(a, &tmX, lf, 0, (int32_t)u.x_row0, k);
-                            tma_load_3d_pair(b, &tmY, lf, 0, y0, k);
+                            if (P.y3d)
+                                tma_load_4d_pair(b, &tmY, lf, 0, y0, k, u.batch);
+                            else
+                                tma_load_3d_pair(b, &tmY, lf, 0, y0, k);
                         }
                     } else if (leader) {
                         mbar_arrive_expect_tx(&full[s], 2 * (Cfg::A_BYTES + Cfg::B_BYTES));

@@ -107,6 +107,22 @@ def test_grouped_ragged(lib, counts):
     assert_close(D.double().cpu().numpy(), ref, bound, gp.d_type, f"grouped {counts}")
 
 
+@pytest.mark.parametrize("bn", [224, 256])
+@pytest.mark.parametrize("counts,K", [([3, 0, 130, 300, 0, 257], 320), ([256, 1, 0, 511, 129], 72 * 4),
+                                      ([0, 0, 700], 64 * 5), ([40] * 8, 256)])
+def test_grouped_on_cta_pairs(lib, bn, counts, K, monkeypatch):
+    # 256-row expert blocks over CTA pairs: a block's second half may hold
+    # none of its expert's rows; K a multiple of 64 copies two K-steps per box
+    monkeypatch.setenv("GEMM_FORCE_KERNEL", f"umma2_grouped_bn{bn}/dp")
+    gp = synth.grouped(counts, 600, K, seed=len(counts) + bn)
+    rc, D = run_grouped(lib, gp)
+    assert rc == 0, qg.gemm_status_string(rc)
+    assert qg.gemm_last_choice(lib.h) == f"umma2_grouped_bn{bn}/dp"
+    ref, bound = oracle.grouped(gp)
+    assert_close(D.double().cpu().numpy(), ref, bound, gp.d_type, f"grouped pairs bn{bn} {counts}")
+    assert qg.gemm_device_status(lib.h, qg.current_stream()) == 0
+
+
 def test_config5_grouped_full_sampled(lib):
     gp = synth.config5()
     rc, D = run_grouped(lib, gp)
