@@ -298,6 +298,18 @@ int pair_kchunks(const Problem& p) {
     return want;
 }
 
+// K-steps the single-CTA kernel copies per TMA box: two when K is a multiple
+// of 64, the problem is not batched and three stages of two K-steps still fit
+// (tiles up to 128 wide); else one (GEMM_KS=1 forces one).
+int single_kchunks(const Problem& p, const Choice& c) {
+    static const bool allowed = [] {
+        const char* e = getenv("GEMM_KS");
+        return !(e && e[0] == '1');
+    }();
+    if (!allowed || p.K % 64 != 0 || p.batches != 1 || p.K < 64 || p.family != FAM_DENSE) return 1;
+    return umma_max_stages(c.bn, 2) >= 3 ? 2 : 1;
+}
+
 int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_workspace_t* ws, cudaStream_t st) {
     GemmKernelParams kp;
     memset(&kp, 0, sizeof kp);
@@ -356,6 +368,14 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
             rc = make_map(h, &ty, p.B, p.b_type, p.K, p.N, p.ldb, p.num_experts, p.b_bs, c.pair ? c.bn / 2 : c.bn);
         kp.x3d = 0;
         kp.y3d = 1;
+    } else if (!c.pair && !dq && single_kchunks(p, c) > 1) {
+        // two K-steps per copy: X is B (rows N) when swapped, else A
+        const void* X = c.swap ? p.B : p.A;
+        const void* Y = c.swap ? p.A : p.B;
+        rc = make_map_kchunk(h, &tx, X, p.a_type, p.K, c.swap ? p.N : p.M, c.swap ? p.ldb : p.lda, 128, 2);
+        if (rc == GEMM_OK) rc = make_map_kchunk(h, &ty, Y, p.a_type, p.K, c.swap ? p.M : p.N, c.swap ? p.lda : p.ldb, c.bn, 2);
+        kp.x3d = kp.y3d = 0;
+        kp.ks = 2;
     } else if (c.swap) {
         rc = s4 ? make_map_s4(h, &tx, p.B, p.K, p.N, p.ldb, 128) : make_map(h, &tx, p.B, p.b_type, p.K, p.N, p.ldb, 1, 0, 128);
         if (rc == GEMM_OK) rc = make_map(h, &ty, p.A, p.a_type, p.K, p.M, p.lda, 1, 0, c.bn);
@@ -435,7 +455,7 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
         return ce == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
     if (kp.ks == 0) kp.ks = 1;
-    kp.stages = c.pair ? umma_pair_max_stages(c.bn, kp.ks) : umma_max_stages(c.bn);
+    kp.stages = c.pair ? umma_pair_max_stages(c.bn, kp.ks) : umma_max_stages(c.bn, kp.ks);
     if (kp.stages < 2) return GEMM_ERR_NO_KERNEL;
     if (const char* fs = getenv("GEMM_STAGES")) {  // ring depth override for tuning sweeps
         const int want = atoi(fs);

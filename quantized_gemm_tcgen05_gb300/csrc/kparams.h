@@ -73,7 +73,7 @@ struct GemmKernelParams {
     uint32_t* status;     // device status words [4]
     uint64_t timeout_ns;  // bound on every wait
     int32_t pair;         // CTA-pair kernel: units are 256-row tiles shared by the two CTAs of a cluster
-    int32_t ks;           // CTA-pair kernel: 64-wide K-steps per stage (>1: X/Y maps index 64-wide K chunks)
+    int32_t ks;           // 64-wide K-steps per stage (>1: X/Y maps index 64-wide K chunks)
 };
 
 // Instruction descriptor of tcgen05.mma.kind::f16: fp32 accumulator (bits
@@ -102,7 +102,7 @@ struct GemmMaps {
 template <int BN>
 cudaError_t launch_umma_bn(const GemmMaps& m, const GemmKernelParams& p, int grid, cudaStream_t st);
 template <int BN>
-int umma_stages_bn();
+int umma_stages_bn(int ks);
 template <int BN>
 cudaError_t launch_dq_bn(const GemmMaps& m, const GemmKernelParams& p, int grid, cudaStream_t st);
 template <int BN>
@@ -119,7 +119,7 @@ cudaError_t launch_umma_dq_gemm(int bn, const GemmMaps& maps, const GemmKernelPa
                                 cudaStream_t st);
 cudaError_t launch_scale_c(const EpiParams& e, int64_t batches, cudaStream_t st);
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t timeout_ns, cudaStream_t st);
-int umma_max_stages(int bn);
+int umma_max_stages(int bn, int ks);
 cudaError_t launch_umma_pair_gemm(int bn, const GemmMaps& maps, const GemmKernelParams& p, int grid, cudaStream_t st);
 int umma_pair_max_stages(int bn, int ks);
 int umma_pair_max_clusters(int bn);

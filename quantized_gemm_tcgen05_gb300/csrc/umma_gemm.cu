@@ -47,10 +47,10 @@ cudaError_t launch_umma_gemm(int bn, const GemmMaps& m, const GemmKernelParams& 
     }
 }
 
-int umma_max_stages(int bn) {
+int umma_max_stages(int bn, int ks) {
     switch (bn) {
 #define QG_CASE(B) \
-    case B: return umma_stages_bn<B>();
+    case B: return umma_stages_bn<B>(ks);
         QG_FOR_EACH_DENSE_BN(QG_CASE)
 #undef QG_CASE
         default: return 0;

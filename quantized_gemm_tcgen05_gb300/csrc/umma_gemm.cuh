@@ -39,10 +39,11 @@ struct UmmaCfg {
     static constexpr int MAX_STAGES = 16;
     static constexpr uint32_t AUX_BYTES = (2 * MAX_STAGES + 6 + EPI_CBARS) * 8 + 16;
     static constexpr uint32_t FIXED_BYTES = 1024 /*alignment slack*/ + STAGING_BYTES + AUX_BYTES;
-    static size_t smem_bytes(int stages) { return FIXED_BYTES + (size_t)stages * STAGE_BYTES; }
-    static int max_stages() {
+    // a stage holds ks 64-wide K-steps of both operands
+    static size_t smem_bytes(int stages, int ks) { return FIXED_BYTES + (size_t)stages * ks * STAGE_BYTES; }
+    static int max_stages(int ks) {
         const size_t budget = 232448;  // 227 KB opt-in shared memory per block
-        int s = (int)((budget - FIXED_BYTES) / STAGE_BYTES);
+        int s = (int)((budget - FIXED_BYTES) / (ks * STAGE_BYTES));
         return s > MAX_STAGES ? MAX_STAGES : s;
     }
 };
@@ -56,9 +57,12 @@ __global__ void __launch_bounds__(192, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = P.stages;
+    const int KS = P.ks;  // K-steps per stage: 1, or 2 with K-chunk tensor maps (one box per operand per stage)
+    const uint32_t stage_bytes = (uint32_t)KS * Cfg::STAGE_BYTES;
+    const uint32_t a_region = (uint32_t)KS * Cfg::A_BYTES;
     uint8_t* ring = smem;
-    float* staging = reinterpret_cast<float*>(smem + (size_t)S * Cfg::STAGE_BYTES);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * Cfg::STAGE_BYTES + Cfg::STAGING_BYTES);
+    float* staging = reinterpret_cast<float*>(smem + (size_t)S * stage_bytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * stage_bytes + Cfg::STAGING_BYTES);
     uint64_t* empty = full + Cfg::MAX_STAGES;
     uint64_t* tfull = empty + Cfg::MAX_STAGES;
     uint64_t* tempty = tfull + 2;
@@ -114,22 +118,29 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t ph = 0, armed = 0, armed_par = 0;
             bool ok = true;
             while (ok && w.next(P.sched, blockIdx.x, BM, BN, u)) {
-                for (int k = u.k_begin; k < u.k_end; ++k) {
+                for (int k = u.k_begin; k < u.k_end; k += KS) {
                     if (!wait_bar(&empty[s], ph ^ 1, g, SITE_PRODUCER_EMPTY)) {
                         ok = false;
                         break;
                     }
-                    uint8_t* a = ring + (size_t)s * Cfg::STAGE_BYTES;
-                    uint8_t* b = a + Cfg::A_BYTES;
-                    mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
-                    if (P.x3d)
-                        tma_load_3d(a, &tmX, &full[s], k * BK, (int32_t)u.x_row0, u.batch);
-                    else
-                        tma_load_2d(a, &tmX, &full[s], k * BK, (int32_t)u.x_row0);
-                    if (P.y3d)
-                        tma_load_3d(b, &tmY, &full[s], k * BK, (int32_t)u.y_row0, u.batch);
-                    else
-                        tma_load_2d(b, &tmY, &full[s], k * BK, (int32_t)u.y_row0);
+                    uint8_t* a = ring + (size_t)s * stage_bytes;
+                    uint8_t* b = a + a_region;
+                    mbar_arrive_expect_tx(&full[s], stage_bytes);
+                    if (KS > 1) {
+                        // K-chunk maps: coordinates (0, row, chunk); past the
+                        // last chunk TMA fills zeros and still counts the bytes
+                        tma_load_3d(a, &tmX, &full[s], 0, (int32_t)u.x_row0, k);
+                        tma_load_3d(b, &tmY, &full[s], 0, (int32_t)u.y_row0, k);
+                    } else {
+                        if (P.x3d)
+                            tma_load_3d(a, &tmX, &full[s], k * BK, (int32_t)u.x_row0, u.batch);
+                        else
+                            tma_load_2d(a, &tmX, &full[s], k * BK, (int32_t)u.x_row0);
+                        if (P.y3d)
+                            tma_load_3d(b, &tmY, &full[s], k * BK, (int32_t)u.y_row0, u.batch);
+                        else
+                            tma_load_2d(b, &tmY, &full[s], k * BK, (int32_t)u.y_row0);
+                    }
                     armed |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
                     if (++s == S) {
@@ -158,18 +169,21 @@ __global__ void __launch_bounds__(192, 1)
                 if (!wait_bar(&tempty[buf], aph ^ 1, g, SITE_MMA_TMEM_EMPTY)) break;
                 tc_fence_after_sync();
                 const uint32_t d = tmem_base + (uint32_t)(buf * BN);
-                for (int k = u.k_begin; k < u.k_end; ++k) {
+                for (int k = u.k_begin; k < u.k_end; k += KS) {
                     if (!wait_bar(&full[s], ph, g, SITE_MMA_FULL)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a_addr = smem_u32(ring + (size_t)s * Cfg::STAGE_BYTES);
-                    const uint64_t ad = make_sw128_kmajor_desc(a_addr);
-                    const uint64_t bd = make_sw128_kmajor_desc(a_addr + Cfg::A_BYTES);
+                    const uint32_t a_addr = smem_u32(ring + (size_t)s * stage_bytes);
+                    const int nk = u.k_end - k < KS ? u.k_end - k : KS;
+                    for (int h = 0; h < nk; ++h) {
+                        const uint64_t ad = make_sw128_kmajor_desc(a_addr + h * Cfg::A_BYTES);
+                        const uint64_t bd = make_sw128_kmajor_desc(a_addr + a_region + h * Cfg::B_BYTES);
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk)
-                        umma_f16_ss(d, ad + 2 * kk, bd + 2 * kk, P.idesc, (k > u.k_begin || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                            umma_f16_ss(d, ad + 2 * kk, bd + 2 * kk, P.idesc, (k + h > u.k_begin || kk > 0) ? 1u : 0u);
+                    }
                     issued = true;
                     umma_commit(&empty[s]);
                     if (++s == S) {
@@ -186,7 +200,7 @@ __global__ void __launch_bounds__(192, 1)
             }
         }
     } else {
-        const FixupSmem fx{ring, (uint32_t)((size_t)S * Cfg::STAGE_BYTES), fixbar};
+        const FixupSmem fx{ring, (uint32_t)((size_t)S * stage_bytes), fixbar};
         epilogue<BN>(P, &tmC, &tmD, tmem_base, tfull, tempty, reinterpret_cast<uint8_t*>(staging), cbar, bcast, fx, g);
     }
 
@@ -201,7 +215,7 @@ __global__ void __launch_bounds__(192, 1)
 
 template <int BN>
 cudaError_t launch_umma_bn(const GemmMaps& m, const GemmKernelParams& p, int grid, cudaStream_t st) {
-    const size_t smem = UmmaCfg<BN>::smem_bytes(p.stages);
+    const size_t smem = UmmaCfg<BN>::smem_bytes(p.stages, p.ks);
     // raise the dynamic shared-memory limit once per device (to the largest ring)
     static std::atomic<uint64_t> configured{0};
     int dev = 0;
@@ -209,8 +223,7 @@ cudaError_t launch_umma_bn(const GemmMaps& m, const GemmKernelParams& p, int gri
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(configured.load() & bit)) {
-        e = cudaFuncSetAttribute(umma_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)UmmaCfg<BN>::smem_bytes(UmmaCfg<BN>::max_stages()));
+        e = cudaFuncSetAttribute(umma_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
@@ -218,8 +231,8 @@ cudaError_t launch_umma_bn(const GemmMaps& m, const GemmKernelParams& p, int gri
 }
 
 template <int BN>
-int umma_stages_bn() {
-    return UmmaCfg<BN>::max_stages();
+int umma_stages_bn(int ks) {
+    return UmmaCfg<BN>::max_stages(ks);
 }
 
 }  // namespace qg

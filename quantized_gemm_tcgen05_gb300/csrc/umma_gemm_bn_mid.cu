@@ -4,7 +4,7 @@
 
 namespace qg {
 template cudaError_t launch_umma_bn<128>(const GemmMaps&, const GemmKernelParams&, int, cudaStream_t);
-template int umma_stages_bn<128>();
+template int umma_stages_bn<128>(int);
 template cudaError_t launch_umma_bn<192>(const GemmMaps&, const GemmKernelParams&, int, cudaStream_t);
-template int umma_stages_bn<192>();
+template int umma_stages_bn<192>(int);
 }  // namespace qg

@@ -4,9 +4,9 @@
 
 namespace qg {
 template cudaError_t launch_umma_bn<16>(const GemmMaps&, const GemmKernelParams&, int, cudaStream_t);
-template int umma_stages_bn<16>();
+template int umma_stages_bn<16>(int);
 template cudaError_t launch_umma_bn<32>(const GemmMaps&, const GemmKernelParams&, int, cudaStream_t);
-template int umma_stages_bn<32>();
+template int umma_stages_bn<32>(int);
 template cudaError_t launch_umma_bn<64>(const GemmMaps&, const GemmKernelParams&, int, cudaStream_t);
-template int umma_stages_bn<64>();
+template int umma_stages_bn<64>(int);
 }  // namespace qg

@@ -4,7 +4,7 @@
 
 namespace qg {
 template cudaError_t launch_umma_bn<224>(const GemmMaps&, const GemmKernelParams&, int, cudaStream_t);
-template int umma_stages_bn<224>();
+template int umma_stages_bn<224>(int);
 template cudaError_t launch_umma_bn<256>(const GemmMaps&, const GemmKernelParams&, int, cudaStream_t);
-template int umma_stages_bn<256>();
+template int umma_stages_bn<256>(int);
 }  // namespace qg
