@@ -298,16 +298,19 @@ int pair_kchunks(const Problem& p) {
     return want;
 }
 
-// K-steps the single-CTA kernel copies per TMA box: two when K is a multiple
-// of 64, the problem is not batched and three stages of two K-steps still fit
-// (tiles up to 128 wide); else one (GEMM_KS=1 forces one).
+// K-steps the single-CTA kernel copies per TMA box: up to GEMM_KS (default 2,
+// at most 3) when K is a multiple of 64, the problem is not batched and three
+// stages of that many K-steps still fit; else one.
 int single_kchunks(const Problem& p, const Choice& c) {
-    static const bool allowed = [] {
+    static const int want = [] {
         const char* e = getenv("GEMM_KS");
-        return !(e && e[0] == '1');
+        const int v = e ? atoi(e) : 2;
+        return v >= 1 && v <= 3 ? v : 2;
     }();
-    if (!allowed || p.K % 64 != 0 || p.batches != 1 || p.K < 64 || p.family != FAM_DENSE) return 1;
-    return umma_max_stages(c.bn, 2) >= 3 ? 2 : 1;
+    if (p.K % 64 != 0 || p.batches != 1 || p.K < 64 || p.family != FAM_DENSE) return 1;
+    for (int ks = want; ks > 1; --ks)
+        if (umma_max_stages(c.bn, ks) >= 3) return ks;
+    return 1;
 }
 
 int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_workspace_t* ws, cudaStream_t st) {
@@ -369,13 +372,15 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
         kp.x3d = 0;
         kp.y3d = 1;
     } else if (!c.pair && !dq && single_kchunks(p, c) > 1) {
-        // two K-steps per copy: X is B (rows N) when swapped, else A
+        // several K-steps per copy: X is B (rows N) when swapped, else A
         const void* X = c.swap ? p.B : p.A;
         const void* Y = c.swap ? p.A : p.B;
-        rc = make_map_kchunk(h, &tx, X, p.a_type, p.K, c.swap ? p.N : p.M, c.swap ? p.ldb : p.lda, 128, 2);
-        if (rc == GEMM_OK) rc = make_map_kchunk(h, &ty, Y, p.a_type, p.K, c.swap ? p.M : p.N, c.swap ? p.lda : p.ldb, c.bn, 2);
+        const int ks = single_kchunks(p, c);
+        rc = make_map_kchunk(h, &tx, X, p.a_type, p.K, c.swap ? p.N : p.M, c.swap ? p.ldb : p.lda, 128, ks);
+        if (rc == GEMM_OK)
+            rc = make_map_kchunk(h, &ty, Y, p.a_type, p.K, c.swap ? p.M : p.N, c.swap ? p.lda : p.ldb, c.bn, ks);
         kp.x3d = kp.y3d = 0;
-        kp.ks = 2;
+        kp.ks = ks;
     } else if (c.swap) {
         rc = s4 ? make_map_s4(h, &tx, p.B, p.K, p.N, p.ldb, 128) : make_map(h, &tx, p.B, p.b_type, p.K, p.N, p.ldb, 1, 0, 128);
         if (rc == GEMM_OK) rc = make_map(h, &ty, p.A, p.a_type, p.K, p.M, p.lda, 1, 0, c.bn);
