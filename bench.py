@@ -147,20 +147,19 @@ def profile_traffic(cfg, choice):
     or None when it is missing, was taken on other kernel sources, or on
     another kernel choice than the one this run dispatched."""
     import glob
-    found = sorted(glob.glob(os.path.join(ROOT, "profiles", f"*_{cfg}.md")))
-    if not found:
-        return None
-    text = open(found[0]).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    s = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
-    f = re.search(r"kernel_sources:\s*(.+)", text)
-    files = f.group(1).split() if f else None
-    c = re.search(r"kernel_choice:\s*(\S+)", text)
-    if not m or not s or s.group(1) != kernel_source_hash(files):
-        return None
-    if c and c.group(1) != choice:
-        return None
-    return float(m.group(1))
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", f"*_{cfg}.md"))):
+        text = open(path).read()
+        m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+        s = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+        f = re.search(r"kernel_sources:\s*(.+)", text)
+        files = f.group(1).split() if f else None
+        c = re.search(r"kernel_choice:\s*(\S+)", text)
+        if not m or not s or s.group(1) != kernel_source_hash(files):
+            continue
+        if c and c.group(1) != choice:
+            continue
+        return float(m.group(1))
+    return None
 
 
 # ---- clocks -------------------------------------------------------------------------------

@@ -18,6 +18,7 @@
 #include <vector>
 
 #include "dispatch.h"
+#include "gemv.h"
 #include "handle_internal.h"
 #include "kparams.h"
 
@@ -313,7 +314,39 @@ int single_kchunks(const Problem& p, const Choice& c) {
     return 1;
 }
 
+// The small-M streaming kernel: no workspace, no tensor maps.
+int launch_gemv_choice(gemm_handle* h, const Problem& p, cudaStream_t st) {
+    GemvParams g;
+    memset(&g, 0, sizeof g);
+    g.A = p.A;
+    g.B = p.B;
+    g.V = p.V;
+    g.C = p.beta != 0.0f ? p.C : nullptr;
+    g.D = p.D;
+    g.lda = p.lda;
+    g.ldb = p.ldb;
+    g.ldv = p.ldv;
+    g.ldc = p.ldc;
+    g.ldd = p.ldd;
+    g.M = p.M;
+    g.N = p.N;
+    g.K = p.K;
+    g.alpha = p.alpha;
+    g.beta = p.beta;
+    g.a_bf16 = p.a_type == GEMM_BF16;
+    g.b_int4 = p.b_type == GEMM_S4;
+    g.v_bf16 = p.v_type == GEMM_BF16;
+    g.gb = p.V ? p.gb : 0;
+    g.d_type = p.d_type;
+    // enough warps for the weight stream: about 24 per SM
+    g.kslices = gemv_kslices(p.N, p.K, g.b_int4, (int64_t)h->sm_count * 24);
+    const cudaError_t e = launch_gemv(g, h->sm_count, st);
+    if (e == cudaErrorInvalidValue) return GEMM_ERR_NO_KERNEL;
+    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
 int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_workspace_t* ws, cudaStream_t st) {
+    if (c.gemv) return launch_gemv_choice(h, p, st);
     GemmKernelParams kp;
     memset(&kp, 0, sizeof kp);
     if (c.pair && capacity(h, c) < 2) return GEMM_ERR_NO_KERNEL;
@@ -477,6 +510,7 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
 }
 
 bool workspace_fits(gemm_handle* h, const Problem& p, const Choice& c, const gemm_workspace_t* ws) {
+    if (c.gemv) return true;
     SchedParams s = make_sched(p, c, capacity(h, c));
     const size_t need_p = partials_bytes_needed(s, c.bn, c.pair), need_c = counters_bytes_needed(s, c.pair);
     if (!need_p && !need_c) return true;
@@ -515,6 +549,13 @@ float measure(gemm_handle* h, const Problem& p, const Choice& c, const gemm_work
 bool forced_kernel(const Problem& p, Choice* out) {
     const char* f = getenv("GEMM_FORCE_KERNEL");
     if (!f || !*f) return false;
+    if (strcmp(f, "gemv") == 0) {
+        if (!gemv_eligible(p)) return false;
+        *out = Choice();
+        out->bn = 128;
+        out->gemv = 1;
+        return true;
+    }
     const char* bn = strstr(f, "bn");
     const char* slash = strchr(f, '/');
     if (!bn || !slash) return false;
@@ -601,7 +642,7 @@ int dispatch_and_run(gemm_handle* h, const gemm_op_t* op, Problem& p, const gemm
         }
     }
     if (!have) {
-        c = heuristic(p, h->sm_count, ws && ws->partials ? ws->partials_size : 0);
+        c = heuristic(p, h->sm_count, ws && ws->partials ? ws->partials_size : 0, !forced);
         if (forced_split > 1) {
             c.sched = SCHED_SPLITK;
             c.splits = forced_split;

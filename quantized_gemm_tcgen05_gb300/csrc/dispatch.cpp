@@ -2,6 +2,8 @@
 // format.  Host only.
 #include "dispatch.h"
 
+#include <stdlib.h>
+
 #include <math.h>
 #include <stdio.h>
 #include <string.h>
@@ -120,8 +122,31 @@ static bool swap_allowed(const Problem& p) {
     return (p.family == FAM_DENSE || p.family == FAM_DQ) && p.batches == 1 && p.M <= 128;
 }
 
+bool gemv_eligible(const Problem& p) {
+    if (p.family != FAM_DENSE && p.family != FAM_DQ) return false;
+    if (p.batches != 1 || p.M < 1 || p.M > 8 || p.U != nullptr) return false;
+    return p.K / 8 < (int64_t(1) << 24);
+}
+
+// Largest M the heuristic sends to the streaming kernel (GEMM_GEMV_MAX_M
+// overrides the measured default of 2; 0 switches it off).  On GB300 it beats
+// the tensor-core decode path at M = 1 (bf16 N 4096 K 14336: 22 vs 26 us;
+// W4A16 N 11008 K 4096: 17 vs 27 us), ties at M = 2 and loses from M = 4.
+static int64_t gemv_max_m() {
+    const char* v = getenv("GEMM_GEMV_MAX_M");
+    return v ? atoll(v) : 2;
+}
+
+static Choice gemv_choice() {
+    Choice c;
+    c.bn = 128;  // unused; a valid width keeps cache entries uniform
+    c.gemv = 1;
+    return c;
+}
+
 std::vector<Choice> candidates(const Problem& p, int sm_count) {
     std::vector<Choice> out;
+    if (gemv_eligible(p)) out.push_back(gemv_choice());
     const int64_t k_iters = ceil_div(p.K, BK_HOST);
     auto add_scheds = [&](int32_t bn, int32_t swap) {
         Choice c;
@@ -176,11 +201,12 @@ std::vector<Choice> candidates(const Problem& p, int sm_count) {
     return out;
 }
 
-Choice heuristic(const Problem& p, int sm_count, size_t partials_bytes) {
+Choice heuristic(const Problem& p, int sm_count, size_t partials_bytes, bool allow_gemv) {
     // Measured on GB300 (152 SMs): full-width 128 x 256 tiles win whenever
     // there are at least as many tiles as SMs; below that, K is split so all
     // SMs stream -- into as many equal slices as fill one wave (split-K),
     // else by stream-K.
+    if (allow_gemv && gemv_eligible(p) && p.M <= gemv_max_m()) return gemv_choice();
     Choice c;
     if (swap_allowed(p) && p.M <= 64) {
         c.swap = 1;
@@ -260,6 +286,7 @@ Choice heuristic(const Problem& p, int sm_count, size_t partials_bytes) {
 }
 
 std::string choice_name(const Problem& p, const Choice& c) {
+    if (c.gemv) return "gemv";
     char buf[96];
     const char* fam = p.family == FAM_DQ
                           ? "umma_dq"
@@ -274,10 +301,10 @@ std::string choice_name(const Problem& p, const Choice& c) {
 
 // ---- cache text format ------------------------------------------------------------
 //
-//   qgemm-dispatch-cache 2
+//   qgemm-dispatch-cache 3
 //   device <name, spaces as '_'> sm <count> cc <major*10+minor>
 //   entries <n>
-//   <family> <a> <b> <d> <has_c> <has_u> <has_v> <ga> <gb> <m_bucket> <N> <K> <batches> : <bn> <swap> <sched> <splits> <pair> <us>
+//   <family> <a> <b> <d> <has_c> <has_u> <has_v> <ga> <gb> <m_bucket> <N> <K> <batches> : <bn> <swap> <sched> <splits> <pair> <gemv> <us>
 //   ...
 //   end
 
@@ -290,7 +317,7 @@ static std::string sanitize(const std::string& s) {
 
 std::string cache_serialize(const std::map<Key, Choice>& cache, const std::string& device, int sm, int cc) {
     std::ostringstream os;
-    os << "qgemm-dispatch-cache 2\n";
+    os << "qgemm-dispatch-cache 3\n";
     os << "device " << sanitize(device) << " sm " << sm << " cc " << cc << "\n";
     os << "entries " << cache.size() << "\n";
     for (const auto& kv : cache) {
@@ -301,7 +328,7 @@ std::string cache_serialize(const std::map<Key, Choice>& cache, const std::strin
         os << k.family << ' ' << k.a_type << ' ' << k.b_type << ' ' << k.d_type << ' ' << k.has_c << ' ' << k.has_u
            << ' ' << k.has_v << ' ' << k.ga << ' ' << k.gb << ' ' << k.m_bucket << ' ' << k.N << ' ' << k.K << ' '
            << k.batches << " : " << c.bn << ' ' << c.swap << ' ' << c.sched << ' ' << c.splits << ' ' << c.pair << ' '
-           << us
+           << c.gemv << ' ' << us
            << "\n";
     }
     os << "end\n";
@@ -313,6 +340,9 @@ static bool valid_choice(const Key& k, const Choice& c) {
     if (!bn_ok || (c.swap != 0 && c.swap != 1) || c.sched < SCHED_DP || c.sched > SCHED_STREAMK) return false;
     if (c.splits < 1 || c.splits > 64 || !(c.us >= 0.0f)) return false;
     if (c.pair != 0 && c.pair != 1) return false;
+    if (c.gemv != 0 && c.gemv != 1) return false;
+    if (c.gemv && (c.pair || c.swap || (k.family != FAM_DENSE && k.family != FAM_DQ) || k.m_bucket > 8 || k.has_u))
+        return false;
     if (c.pair && (c.swap || c.sched == SCHED_SPLITK || (k.family != FAM_DENSE && k.family != FAM_GROUPED))) return false;
     if (c.pair && c.bn != 128 && c.bn != 224 && c.bn != 256) return false;
     if (k.family < FAM_DENSE || k.family > FAM_GROUPED) return false;
@@ -325,7 +355,7 @@ bool cache_parse(const std::string& text, const std::string& device, int sm, int
     std::string magic, word, dev;
     int version = 0, sm_in = -1, cc_in = -1;
     long long n = -1;
-    if (!(is >> magic >> version) || magic != "qgemm-dispatch-cache" || version != 2) return false;
+    if (!(is >> magic >> version) || magic != "qgemm-dispatch-cache" || version != 3) return false;
     if (!(is >> word) || word != "device" || !(is >> dev)) return false;
     if (!(is >> word) || word != "sm" || !(is >> sm_in)) return false;
     if (!(is >> word) || word != "cc" || !(is >> cc_in)) return false;
@@ -338,7 +368,7 @@ bool cache_parse(const std::string& text, const std::string& device, int sm, int
         std::string colon;
         long long mb, N, K;
         if (!(is >> k.family >> k.a_type >> k.b_type >> k.d_type >> k.has_c >> k.has_u >> k.has_v >> k.ga >> k.gb >>
-              mb >> N >> K >> k.batches >> colon >> c.bn >> c.swap >> c.sched >> c.splits >> c.pair >> c.us))
+              mb >> N >> K >> k.batches >> colon >> c.bn >> c.swap >> c.sched >> c.splits >> c.pair >> c.gemv >> c.us))
             return false;
         if (colon != ":") return false;
         k.m_bucket = mb;

@@ -41,6 +41,7 @@ struct Choice {
     int32_t sched = 0;   // SchedKind
     int32_t splits = 1;  // split-K slices (SCHED_SPLITK)
     int32_t pair = 0;    // CTA-pair kernel: 256 x bn tiles over clusters of two SMs
+    int32_t gemv = 0;    // small-M streaming kernel on the CUDA cores (the fields above unused)
     float us = 0.0f;     // measured time, 0 if never measured
 };
 
@@ -64,10 +65,16 @@ SchedParams make_sched(const Problem& p, const Choice& c, int sm_count);
 size_t partials_bytes_needed(const SchedParams& s, int bn, int pair);
 size_t counters_bytes_needed(const SchedParams& s, int pair);
 
+// The small-M streaming kernel takes the problem: M <= 8, one batch, no U
+// scale, B 16-bit or int4 (with or without V).
+bool gemv_eligible(const Problem& p);
+
 // Every kernel variant that can run the problem.
 std::vector<Choice> candidates(const Problem& p, int sm_count);
 // The choice made without measuring.
-Choice heuristic(const Problem& p, int sm_count, size_t partials_bytes);
+// allow_gemv: false when the caller asked for a K split (or for none): those
+// name schedules of the tensor-core kernels.
+Choice heuristic(const Problem& p, int sm_count, size_t partials_bytes, bool allow_gemv = true);
 std::string choice_name(const Problem& p, const Choice& c);
 
 // Cache text format (see dispatch.cpp).

@@ -65,6 +65,33 @@ def test_w4a16_small(lib, M, N):
         assert_close(D.double().cpu().numpy(), ref, bound, p.d_type, f"W4A16 {M}x{N}x{K} g{group}")
 
 
+@pytest.mark.parametrize("group,K", [(8, 256), (16, 448), (32, 224), (64, 832), (192, 768), (256, 1280)])
+@pytest.mark.parametrize("sched", ["auto", "streamk", "splitk3"])
+def test_int4_groups_and_slot_edges(lib, group, K, sched):
+    # int4 rows and their scale rows arrive four K-steps at a time: split-K
+    # and stream-K units start and end inside such a chunk, groups under 64
+    # need several scale rows per K-step, a group of 192 straddles chunks,
+    # and K = 224 ends half-way through a K-step
+    M, N = 128, 384
+    p = synth.w4a16(M, N, K, seed=group + K, group=group)
+    o = {"auto": op(gb=group), "streamk": op(streamk=1, gb=group), "splitk3": op(splitk=3, gb=group)}[sched]
+    rc, D = run_problem(lib, p, o)
+    assert rc == 0, f"status {rc}"
+    ref, bound = oracle.gemm(p)
+    assert_close(D.double().cpu().numpy(), ref, bound, p.d_type, f"W4A16 g{group} K{K} {sched}")
+
+
+@pytest.mark.parametrize("M", [1, 40])
+def test_int4_swapped_groups(lib, M):
+    # decode-sized M: the int4 weights are the 128-row X operand
+    for group, K in ((8, 320), (192, 576), (64, 4096 + 64)):
+        p = synth.w4a16(M, 520, K, seed=M + group, group=group)
+        rc, D = run_problem(lib, p, op(gb=group))
+        assert rc == 0
+        ref, bound = oracle.gemm(p)
+        assert_close(D.double().cpu().numpy(), ref, bound, p.d_type, f"W4A16 swapped M{M} g{group} K{K}")
+
+
 def test_config4_full(lib):
     p = synth.config4()
     rc, D = run_problem(lib, p)

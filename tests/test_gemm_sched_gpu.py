@@ -146,13 +146,13 @@ def test_cache_measure_export_import(lib):
     assert_close(D.double().cpu().numpy(), ref, bound, p.d_type, "measured")
     assert qg.gemm_cache_size(lib.h) == n0 + 1
     blob = qg.gemm_export(lib.h)
-    assert blob.startswith(b"qgemm-dispatch-cache 2\n")
+    assert blob.startswith(b"qgemm-dispatch-cache 3\n")
     h2 = qg.gemm_create()
     try:
         assert qg.gemm_import(h2, blob) == 0
         assert qg.gemm_cache_size(h2) == qg.gemm_cache_size(lib.h)
         assert qg.gemm_export(h2) == blob
-        for bad in (blob[:-5], blob.replace(b"sm ", b"sm 1"), b"qgemm-dispatch-cache 1\n" + blob[23:], b"garbage"):
+        for bad in (blob[:-5], blob.replace(b"sm ", b"sm 1"), b"qgemm-dispatch-cache 2\n" + blob[23:], b"garbage"):
             assert qg.gemm_import(h2, bad) == qg.GEMM_ERR_BAD_CACHE
         assert qg.gemm_export(h2) == blob
     finally:
