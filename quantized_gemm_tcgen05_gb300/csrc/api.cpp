@@ -338,8 +338,13 @@ int launch_gemv_choice(gemm_handle* h, const Problem& p, cudaStream_t st) {
     g.v_bf16 = p.v_type == GEMM_BF16;
     g.gb = p.V ? p.gb : 0;
     g.d_type = p.d_type;
-    // enough warps for the weight stream: about 24 per SM
+    // enough warps for the weight stream: about 24 per SM (GEMM_GEMV_KSLICES
+    // = 1, 2, 4 or 8 overrides the split, for tuning)
     g.kslices = gemv_kslices(p.N, p.K, g.b_int4, (int64_t)h->sm_count * 24);
+    if (const char* ks = getenv("GEMM_GEMV_KSLICES")) {
+        const int v = atoi(ks);
+        if (v == 1 || v == 2 || v == 4 || v == 8) g.kslices = v;
+    }
     const cudaError_t e = launch_gemv(g, h->sm_count, st);
     if (e == cudaErrorInvalidValue) return GEMM_ERR_NO_KERNEL;
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
