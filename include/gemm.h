@@ -213,6 +213,7 @@ int gemm_run_grouped(gemm_handle_t h, const gemm_op_t* op, float alpha,
  * (or cap too small) stores the needed size in *written and returns GEMM_OK
  * (respectively GEMM_ERR_INVALID_ARG).  Import merges the entries of a blob
  * made by Export on a device with the same name and SM count; any other blob
+ * (including one of an older format version: this library writes version 3)
  * returns GEMM_ERR_BAD_CACHE and leaves the cache unchanged.
  */
 int gemm_export(gemm_handle_t h, void* buf, size_t cap, size_t* written);

@@ -115,3 +115,26 @@ def test_heuristic_takes_gemv_for_decode(lib):
     q = synth.config3(16)  # the tensor core keeps up from M = 4 on
     rc, _ = run_problem(lib, q)
     assert rc == 0 and qg.gemm_last_choice(lib.h) != "gemv"
+
+
+def test_measured_choice_round_trips_through_the_cache(lib):
+    # measure mode times the streaming kernel beside the tensor-core ones and
+    # caches the winner; an exported cache makes a fresh handle choose the same
+    p = synth.w4a16(1, 4096, 4096, seed=12)
+    rc, D = run_problem(lib, p, op(dispatch=qg.GEMM_DISPATCH_MEASURE, gb=p.gb))
+    assert rc == 0
+    chosen = qg.gemm_last_choice(lib.h)
+    ref, bound = oracle.gemm(p)
+    assert_close(D.double().cpu().numpy(), ref, bound, p.d_type, "measured W4A16 M=1")
+    blob = qg.gemm_export(lib.h)
+    assert blob.startswith(b"qgemm-dispatch-cache 3\n")
+    h2 = qg.gemm_create()
+    try:
+        assert qg.gemm_import(h2, blob) == 0
+        other = Lib.__new__(Lib)
+        other.h, other.ws = h2, lib.ws
+        rc, D2 = run_problem(other, p, op(gb=p.gb))
+        assert rc == 0 and qg.gemm_last_choice(h2) == chosen
+        assert torch.equal(D, D2)
+    finally:
+        qg.gemm_destroy(h2)
