@@ -92,16 +92,39 @@ enum {
 };
 
 /*
+ * Epilogue flags for gemm_op_t.epilogue: the fused bias + activation of the
+ * DeepGEMM kernel-set blog, section 6.1 (bias, then ReLU or GELU, applied in
+ * the epilogue that writes D).  With x = alpha * acc + beta * c (fp32):
+ *   GEMM_EPILOGUE_BIAS  x += bias[j] (one value per output column j, shared by
+ *                       every row, batch and expert);
+ *   GEMM_EPILOGUE_RELU  x = x < 0 ? 0 : x (NaN stays NaN);
+ *   GEMM_EPILOGUE_GELU  x = x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)), the exact
+ *                       (erf) form;
+ * then D = RN_D(x).  RELU and GELU exclude each other; 0 is the plain
+ * alpha/beta/cast epilogue.
+ */
+enum {
+    GEMM_EPILOGUE_DEFAULT = 0,
+    GEMM_EPILOGUE_BIAS = 1,
+    GEMM_EPILOGUE_RELU = 2,
+    GEMM_EPILOGUE_GELU = 4
+};
+
+/*
  * Operation: "dispatch policy, epilogue, quantization config" (Gemm Interface,
  * I/O Contract).
  */
 typedef struct {
     int32_t dispatch;      /* GEMM_DISPATCH_*                                        */
-    int32_t epilogue;      /* 0: alpha/beta/cast (the only epilogue served)          */
+    int32_t epilogue;      /* GEMM_EPILOGUE_* flags (0: alpha/beta/cast)              */
     int32_t quant_a_group; /* 0: no U; else U's group size along K: 8, 16, 32 or a multiple of 64 */
     int32_t quant_b_group; /* 0: no V; else V's group size along K: 8, 16, 32 or a multiple of 64 */
     int32_t splitk;        /* 0: automatic; 1: unsplit; S > 1: force S K-slices       */
     int32_t streamk;       /* 0: automatic; 1: force stream-K; -1: never stream-K     */
+    const void* bias;      /* GEMM_EPILOGUE_BIAS: N contiguous values on the device,
+                              aligned to their element size, owned by the caller;
+                              ignored otherwise                                       */
+    int32_t bias_type;     /* GEMM_F32 / GEMM_F16 / GEMM_BF16                         */
 } gemm_op_t;
 
 /*

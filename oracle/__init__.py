@@ -57,6 +57,7 @@ class _Gemm(ctypes.Structure):
         ("v_type", ctypes.c_int), ("V", ctypes.c_void_p), ("ldv", ctypes.c_int64), ("gb", ctypes.c_int64),
         ("c_type", ctypes.c_int), ("C", ctypes.c_void_p), ("ldc", ctypes.c_int64),
         ("alpha", ctypes.c_double), ("beta", ctypes.c_double),
+        ("epilogue", ctypes.c_int), ("bias_type", ctypes.c_int), ("bias", ctypes.c_void_p),
     ]
 
 
@@ -161,6 +162,12 @@ def _desc(p, keep):
         keep.append(V)
         g.v_type, g.V, g.ldv, g.gb = p.v_type, V.ctypes.data, p.N, p.gb
     g.alpha, g.beta = float(p.alpha), float(p.beta)
+    g.epilogue = int(getattr(p, "epilogue", 0) or 0)
+    if g.epilogue & 1:
+        bias = np.ascontiguousarray(p.bias)
+        bias = bias.view(np.uint32) if p.bias_type == F32 else bias.astype(np.uint16, copy=False)
+        keep.append(bias)
+        g.bias_type, g.bias = p.bias_type, bias.ctypes.data
     if p.beta != 0.0:
         C = np.ascontiguousarray(p.C)
         C = C.view(np.uint32) if p.c_type == F32 else C.astype(np.uint16, copy=False)
@@ -209,6 +216,8 @@ class _Slice:
         self.alpha, self.beta = gp.alpha, gp.beta
         self.C = None
         self.c_type = None
+        self.epilogue = getattr(gp, "epilogue", 0)
+        self.bias, self.bias_type = getattr(gp, "bias", None), getattr(gp, "bias_type", None)
 
 
 def grouped(gp):

@@ -14,6 +14,10 @@
  *    DeepGEMM kernel-set blog, section 1.1.
  *  - U/V are group-wise scales that advance at K-group boundaries:
  *    "InternLM Lmdeploy Gemm MainloopSm80V2", section Description (GroupIter).
+ *  - The fused epilogue of the DeepGEMM kernel-set blog, section 6.1: a bias
+ *    per output column, then ReLU or GELU, applied to alpha*(A@B) + beta*C.
+ *    GELU is the exact form x * Phi(x) = x/2 * (1 + erf(x / sqrt 2)); ReLU maps
+ *    x < 0 to 0 and keeps NaN.
  *
  * Arithmetic: every operand element is decoded exactly to double; a scaled
  * operand is formed as the exact product with its group scale and rounded once
@@ -23,7 +27,10 @@
  * error, which is what the fp32-accumulating GPU path must approach.
  *
  * Alongside ref[i][j] it returns bound[i][j] = |alpha| * sum_k |a_ik * b_kj|
- * + |beta * c_ij|, the scale against which the GPU tolerance is stated.
+ * + |beta * c_ij| (+ |bias_j|), the scale against which the GPU tolerance is
+ * stated; after GELU it is multiplied by 1.129, the largest slope of x*Phi(x)
+ * (reached at x = sqrt 2: Phi(sqrt 2) + sqrt 2 * phi(sqrt 2) = 1.1289...), so
+ * an error in the pre-activation value stays covered.  ReLU's slope is at most 1.
  *
  * Build: gcc -O2 -fopenmp -shared -fPIC gemm_oracle.c -o liboracle.so -lm
  */
@@ -139,6 +146,8 @@ typedef struct {
     int v_type; const void* V; int64_t ldv; int64_t gb; /* [K/gb][N] or V == 0  */
     int c_type; const void* C; int64_t ldc;             /* M x N row-major      */
     double alpha, beta;
+    int epilogue;               /* bit 0: + bias[j]; bit 1: ReLU; bit 2: GELU     */
+    int bias_type; const void* bias;                    /* N values (bit 0)     */
 } oracle_gemm_t;
 
 static uint32_t load_bits(int type, const void* p, int64_t idx)
@@ -196,6 +205,10 @@ static int check(const oracle_gemm_t* P)
         return 1;
     if (P->beta != 0.0 && !P->C)
         return 1;
+    if ((P->epilogue & 1) && !P->bias)
+        return 1;
+    if ((P->epilogue & 2) && (P->epilogue & 4))
+        return 1;
     return 0;
 }
 
@@ -207,6 +220,17 @@ static void finish(const oracle_gemm_t* P, int64_t i, int64_t j, double s, doubl
         double c = oracle_decode(P->c_type, load_bits(P->c_type, P->C, i * P->ldc + j));
         r += P->beta * c;
         b += fabs(P->beta * c);
+    }
+    if (P->epilogue & 1) {
+        double bj = oracle_decode(P->bias_type, load_bits(P->bias_type, P->bias, j));
+        r += bj;
+        b += fabs(bj);
+    }
+    if (P->epilogue & 2)
+        r = r < 0.0 ? 0.0 : r;
+    if (P->epilogue & 4) {
+        r = 0.5 * r * (1.0 + erf(r / sqrt(2.0)));
+        b *= 1.129;
     }
     *ref = r;
     *bound = b;

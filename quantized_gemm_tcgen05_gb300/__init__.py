@@ -29,6 +29,7 @@ GEMM_ERR_BAD_CACHE = 7
 GEMM_F32, GEMM_F16, GEMM_BF16, GEMM_S4 = 0, 1, 2, 3
 GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
 GEMM_DISPATCH_DEFAULT, GEMM_DISPATCH_MEASURE, GEMM_DISPATCH_REUSE = 0, 1, 2
+GEMM_EPILOGUE_DEFAULT, GEMM_EPILOGUE_BIAS, GEMM_EPILOGUE_RELU, GEMM_EPILOGUE_GELU = 0, 1, 2, 4
 GEMM_BARRIERS_SIZE = 1 << 20
 GEMM_PARTIALS_SIZE = 32 << 20
 GEMM_NOALLOC_BARRIERS_SIZE = 64 << 10
@@ -61,7 +62,8 @@ class gemm_layout_t(ctypes.Structure):
 
 class gemm_op_t(ctypes.Structure):
     _fields_ = [("dispatch", ctypes.c_int32), ("epilogue", ctypes.c_int32), ("quant_a_group", ctypes.c_int32),
-                ("quant_b_group", ctypes.c_int32), ("splitk", ctypes.c_int32), ("streamk", ctypes.c_int32)]
+                ("quant_b_group", ctypes.c_int32), ("splitk", ctypes.c_int32), ("streamk", ctypes.c_int32),
+                ("bias", ctypes.c_void_p), ("bias_type", ctypes.c_int32)]
 
 
 class gemm_workspace_t(ctypes.Structure):

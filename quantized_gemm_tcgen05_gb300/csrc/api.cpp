@@ -56,6 +56,8 @@ bool is16(int32_t t) { return t == GEMM_F16 || t == GEMM_BF16; }
 bool is_float_out(int32_t t) { return t == GEMM_F32 || t == GEMM_F16 || t == GEMM_BF16; }
 static_assert(GEMM_F32 == DT_F32 && GEMM_F16 == DT_F16 && GEMM_BF16 == DT_BF16 && GEMM_S4 == DT_S4,
               "the C ABI's dtype codes are the kernels' codes");
+static_assert(GEMM_EPILOGUE_BIAS == EPI_BIAS && GEMM_EPILOGUE_RELU == EPI_RELU && GEMM_EPILOGUE_GELU == EPI_GELU,
+              "the C ABI's epilogue flags are the kernels' flags");
 
 int64_t elem_bytes_x2(int32_t t) { return t == GEMM_F32 ? 8 : (t == GEMM_S4 ? 1 : 4); }  // 2 * bytes
 
@@ -338,6 +340,9 @@ int launch_gemv_choice(gemm_handle* h, const Problem& p, cudaStream_t st) {
     g.v_bf16 = p.v_type == GEMM_BF16;
     g.gb = p.V ? p.gb : 0;
     g.d_type = p.d_type;
+    g.epi_flags = p.epi_flags;
+    g.bias = p.bias;
+    g.bias_type = p.bias_type;
     // enough warps for the weight stream: about 24 per SM (GEMM_GEMV_KSLICES
     // = 1, 2, 4 or 8 overrides the split, for tuning)
     g.kslices = gemv_kslices(p.N, p.K, g.b_int4, (int64_t)h->sm_count * 24);
@@ -377,6 +382,9 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
     e.alpha = p.alpha;
     e.beta = p.beta;
     e.d_type = p.d_type;
+    e.flags = p.epi_flags;
+    e.bias = p.bias;
+    e.bias_type = p.bias_type;
     e.swap = c.swap;
     const int64_t eb = p.d_type == GEMM_F32 ? 4 : 2;
     e.vec_ok = aligned16(p.D) && (p.ldd * eb) % 16 == 0 &&
@@ -609,6 +617,9 @@ int dispatch_and_run(gemm_handle* h, const gemm_op_t* op, Problem& p, const gemm
         e.alpha = p.alpha;
         e.beta = p.beta;
         e.d_type = p.d_type;
+        e.flags = p.epi_flags;
+        e.bias = p.bias;
+        e.bias_type = p.bias_type;
         h->last_choice = "scale_c";
         return launch_scale_c(e, p.batches, st) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
@@ -682,7 +693,18 @@ int build_problem(gemm_handle* h, const gemm_op_t* op, float alpha, const void* 
                   const void* V, const gemm_layout_t* Vdesc, float beta, const void* C, const gemm_layout_t* Cdesc,
                   void* D, const gemm_layout_t* Ddesc, bool grouped, Problem* out) {
     if (!h || !op || !Adesc || !Bdesc || !Ddesc) return GEMM_ERR_INVALID_ARG;
-    if (op->epilogue != 0) return GEMM_ERR_UNSUPPORTED;
+    // fused epilogue: known flags only, ReLU and GELU exclusive, a bias of a
+    // float type aligned to its element when the bias flag is set
+    if (op->epilogue & ~(GEMM_EPILOGUE_BIAS | GEMM_EPILOGUE_RELU | GEMM_EPILOGUE_GELU)) return GEMM_ERR_INVALID_ARG;
+    if ((op->epilogue & GEMM_EPILOGUE_RELU) && (op->epilogue & GEMM_EPILOGUE_GELU)) return GEMM_ERR_INVALID_ARG;
+    if (op->epilogue & GEMM_EPILOGUE_BIAS) {
+        if (!op->bias) return GEMM_ERR_INVALID_ARG;
+        if (op->bias_type != GEMM_F32 && op->bias_type != GEMM_F16 && op->bias_type != GEMM_BF16)
+            return GEMM_ERR_UNSUPPORTED;
+        const uintptr_t align = op->bias_type == GEMM_F32 ? 4 : 2;
+        if (reinterpret_cast<uintptr_t>(op->bias) % align) return GEMM_ERR_INVALID_ARG;
+        if (!device_pointer(h, op->bias)) return GEMM_ERR_INVALID_ARG;
+    }
     if (op->dispatch < GEMM_DISPATCH_DEFAULT || op->dispatch > GEMM_DISPATCH_REUSE) return GEMM_ERR_INVALID_ARG;
     if (op->splitk < 0 || op->streamk < -1 || op->streamk > 1) return GEMM_ERR_INVALID_ARG;
     if (op->splitk > 1 && op->streamk == 1) return GEMM_ERR_INVALID_ARG;
@@ -705,6 +727,9 @@ int build_problem(gemm_handle* h, const gemm_op_t* op, float alpha, const void* 
     if ((rc = check_layout(Ddesc, GEMM_ROW_MAJOR, p.M, p.N))) return rc;
     p.alpha = alpha;
     p.beta = beta;
+    p.epi_flags = op->epilogue;
+    p.bias = (op->epilogue & GEMM_EPILOGUE_BIAS) ? op->bias : nullptr;
+    p.bias_type = op->bias_type;
     p.A = A;
     p.lda = Adesc->ld;
     p.a_bs = Adesc->batch_stride;

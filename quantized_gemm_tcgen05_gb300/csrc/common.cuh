@@ -3,6 +3,7 @@
 // (TMEM -> registers -> alpha/beta/cast -> global), including the split-K /
 // stream-K partial write and the last-arriver reduction.
 #pragma once
+#include <type_traits>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdlib.h>
@@ -185,8 +186,70 @@ __device__ __forceinline__ void st4(void* p, int32_t t, int64_t i, float4 v) {
     *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p) + i) = raw;
 }
 
-__device__ __forceinline__ float epi_value(const EpiParams& e, float acc, float c) {
-    return e.beta != 0.0f ? fmaf(e.alpha, acc, e.beta * c) : e.alpha * acc;
+// Bias of output column n for the fused epilogue: 0 without the bias flag
+// and for columns past N (a tile's overhang).  Callers load it once per
+// column and chunk, not per element.
+__device__ __forceinline__ float bias_at(const EpiParams& e, int64_t n) {
+    return ((e.flags & EPI_BIAS) && n < e.N) ? ld_elem(e.bias, e.bias_type, n) : 0.0f;
+}
+
+// Bring the bias of a unit's output columns into L1 before its accumulator is
+// ready, so the epilogue's per-chunk bias loads hit L1 (a first touch costs
+// about a microsecond under load).  Lane l prefetches the 128-byte line of
+// columns first + 32 l .. ; 32 lines cover the widest tile (256 columns) and
+// the 128 rows of a swapped one.
+__device__ __forceinline__ void prefetch_bias(const EpiParams& e, int64_t first, int64_t count, int lane) {
+    if (!(e.flags & EPI_BIAS)) return;
+    const int64_t es = e.bias_type == DT_F32 ? 4 : 2;
+    const int64_t per_line = 128 / es;
+    const int64_t n = first + per_line * lane;
+    if (lane * per_line < count && n < e.N) {
+        const char* a = static_cast<const char*>(e.bias) + n * es;
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
+    }
+}
+
+// The fused steps after x = alpha * acc + beta * c: + bias, then ReLU (keeps
+// NaN) or GELU in the exact form x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)).
+__device__ __forceinline__ float epi_finish(const EpiParams& e, float x, float bias) {
+    if (e.flags & EPI_BIAS) x += bias;
+    if (e.flags & EPI_RELU) x = x < 0.0f ? 0.0f : x;
+    if (e.flags & EPI_GELU) x = 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+    return x;
+}
+
+// Compile-time form of the fused steps: -1 none; 0 + bias, then ReLU if its
+// flag is set (a select, not a branch); 2 + bias, GELU (the bias is 0 without
+// the bias flag).  Callers pick it once per chunk, so no element carries a
+// branch: per-element branches on the flags cost a third of C2's time.
+__device__ __forceinline__ int epi_act(const EpiParams& e) {
+    return !e.flags ? -1 : ((e.flags & EPI_GELU) ? 2 : 0);
+}
+
+template <int ACT>
+using EpiAct = std::integral_constant<int, ACT>;
+
+// Run f(EpiAct<act>) for the epilogue's act.
+template <typename F>
+__device__ __forceinline__ void with_epi_act(const EpiParams& e, F&& f) {
+    switch (epi_act(e)) {
+        case -1: f(EpiAct<-1>{}); break;
+        case 0: f(EpiAct<0>{}); break;
+        default: f(EpiAct<2>{}); break;
+    }
+}
+
+// The value stored: alpha * acc + beta * c, then the fused steps of ACT with
+// the column's bias.
+template <int ACT>
+__device__ __forceinline__ float epi_value(const EpiParams& e, float acc, float c, float bias) {
+    float x = e.beta != 0.0f ? fmaf(e.alpha, acc, e.beta * c) : e.alpha * acc;
+    if constexpr (ACT >= 0) {
+        x += bias;
+        if constexpr (ACT == 0) x = ((e.flags & EPI_RELU) && x < 0.0f) ? 0.0f : x;
+        if constexpr (ACT == 2) x = 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+    }
+    return x;
 }
 
 // ---- epilogue --------------------------------------------------------------------------
@@ -270,8 +333,8 @@ __device__ __forceinline__ void load_c_chunk(const EpiParams& e, const Unit& u, 
 // r = ew*32 + lane, combined with the prefetched C values.  `staging` is this
 // warp's private 32 x W fp32 buffer (swizzled by 16-byte quads) that turns the
 // row-per-thread TMEM layout into row-contiguous global stores.
-template <int W>
-__device__ __forceinline__ void store_chunk(const EpiParams& e, const Unit& u, int ew, int lane, int col0,
+template <int W, int ACT>
+__device__ __forceinline__ void store_chunk_t(const EpiParams& e, const Unit& u, int ew, int lane, int col0,
                                             const float (&v)[W], const CChunk<W>& cc, float4* staging) {
     constexpr int Q = W / 4;
     const int64_t boff_d = (int64_t)u.batch * e.d_bstride;
@@ -280,10 +343,11 @@ __device__ __forceinline__ void store_chunk(const EpiParams& e, const Unit& u, i
         // hold consecutive n, so each store instruction is row-contiguous.
         const int64_t n = u.x_row0 + ew * 32 + lane;
         if (n >= e.N || ew * 32 + lane >= u.x_rows) return;
+        const float bn = ACT >= 0 ? bias_at(e, n) : 0.0f;
 #pragma unroll
         for (int j = 0; j < W; ++j) {
             const int64_t m = u.y_row0 + col0 + j;
-            if (m < e.M) st_elem(e.D, e.d_type, boff_d + m * e.ldd + n, epi_value(e, v[j], cc.v[j]));
+            if (m < e.M) st_elem(e.D, e.d_type, boff_d + m * e.ldd + n, epi_value<ACT>(e, v[j], cc.v[j], bn));
         }
         return;
     }
@@ -292,6 +356,13 @@ __device__ __forceinline__ void store_chunk(const EpiParams& e, const Unit& u, i
         staging[lane * Q + (j ^ (lane & (Q - 1)))] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     __syncwarp();
     constexpr int ROWS_PER_IT = 32 / Q;
+    // this lane's quad of columns is the same in every iteration
+    float bq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (ACT >= 0) {
+        const int64_t nq = u.y_row0 + col0 + 4 * (lane % Q);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) bq[t] = bias_at(e, nq + t);
+    }
 #pragma unroll
     for (int it = 0; it < Q; ++it) {
         const int rr = it * ROWS_PER_IT + lane / Q;  // row within this warp's 32
@@ -302,8 +373,10 @@ __device__ __forceinline__ void store_chunk(const EpiParams& e, const Unit& u, i
         const int64_t n0 = u.y_row0 + col0 + 4 * j;
         if (rt >= u.x_rows || m >= e.M || n0 >= e.N) continue;
         const int64_t di = boff_d + m * e.ldd + n0;
-        const float4 o = make_float4(epi_value(e, a.x, cc.v[4 * it]), epi_value(e, a.y, cc.v[4 * it + 1]),
-                                     epi_value(e, a.z, cc.v[4 * it + 2]), epi_value(e, a.w, cc.v[4 * it + 3]));
+        const float4 o = make_float4(epi_value<ACT>(e, a.x, cc.v[4 * it], bq[0]),
+                                     epi_value<ACT>(e, a.y, cc.v[4 * it + 1], bq[1]),
+                                     epi_value<ACT>(e, a.z, cc.v[4 * it + 2], bq[2]),
+                                     epi_value<ACT>(e, a.w, cc.v[4 * it + 3], bq[3]));
         if (e.vec_ok && n0 + 3 < e.N) {
             st4(e.D, e.d_type, di, o);
         } else {
@@ -312,6 +385,12 @@ __device__ __forceinline__ void store_chunk(const EpiParams& e, const Unit& u, i
         }
     }
     __syncwarp();
+}
+
+template <int W>
+__device__ __forceinline__ void store_chunk(const EpiParams& e, const Unit& u, int ew, int lane, int col0,
+                                            const float (&v)[W], const CChunk<W>& cc, float4* staging) {
+    with_epi_act(e, [&](auto act) { store_chunk_t<W, decltype(act)::value>(e, u, ew, lane, col0, v, cc, staging); });
 }
 
 // Partial tile layout in the workspace: for chunk c and quad j, the 128 rows'
@@ -387,6 +466,12 @@ __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uin
     Unit u;
     uint32_t acc_it = 0;
     while (next_unit(P, w, u, BN)) {
+        if (P.epi.flags) {
+            if (P.epi.swap)
+                prefetch_bias(P.epi, u.x_row0 + ew * 32, 32, lane);
+            else
+                prefetch_bias(P.epi, u.y_row0, BN, lane);
+        }
         const int buf = acc_it & 1;
         const uint32_t aph = (acc_it >> 1) & 1;
         ++acc_it;
@@ -598,45 +683,62 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
         if (store) {
             if (f32) {
                 uint8_t* row = buf + lane * 128;
+                const int64_t n0 = slab_x(u, c);
+                auto put = [&](auto act) {
+                    constexpr int F = decltype(act)::value;
+                    // lane l holds the bias of the chunk's column l (W = 32 columns)
+                    const float bl = F >= 0 ? bias_at(e, n0 + lane) : 0.0f;
+                    auto bcol = [&](int col) { return F >= 0 ? __shfl_sync(0xffffffffu, bl, col) : 0.0f; };
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    float4* pp = reinterpret_cast<float4*>(row + ((q ^ (lane & 7)) << 4));
-                    const float4 cv = use_c ? *pp : make_float4(0.f, 0.f, 0.f, 0.f);
-                    *pp = make_float4(epi_value(e, v[4 * q], cv.x), epi_value(e, v[4 * q + 1], cv.y),
-                                      epi_value(e, v[4 * q + 2], cv.z), epi_value(e, v[4 * q + 3], cv.w));
-                }
+                    for (int q = 0; q < 8; ++q) {
+                        float4* pp = reinterpret_cast<float4*>(row + ((q ^ (lane & 7)) << 4));
+                        const float4 cv = use_c ? *pp : make_float4(0.f, 0.f, 0.f, 0.f);
+                        *pp = make_float4(epi_value<F>(e, v[4 * q], cv.x, bcol(4 * q)),
+                                          epi_value<F>(e, v[4 * q + 1], cv.y, bcol(4 * q + 1)),
+                                          epi_value<F>(e, v[4 * q + 2], cv.z, bcol(4 * q + 2)),
+                                          epi_value<F>(e, v[4 * q + 3], cv.w, bcol(4 * q + 3)));
+                    }
+                };
+                with_epi_act(e, put);
             } else {
                 uint8_t* row = buf + lane * 64;
+                const int64_t n0 = slab_x(u, c);
+                auto put = [&](auto act) {
+                    constexpr int F = decltype(act)::value;
+                    const float bl = F >= 0 ? bias_at(e, n0 + lane) : 0.0f;
+                    auto bcol = [&](int col) { return F >= 0 ? __shfl_sync(0xffffffffu, bl, col) : 0.0f; };
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint4* pp = reinterpret_cast<uint4*>(row + ((q ^ ((lane >> 1) & 3)) << 4));
-                    float cv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                    if (use_c) {
-                        const uint4 in = *pp;
-                        const uint32_t iw[4] = {in.x, in.y, in.z, in.w};
+                    for (int q = 0; q < 4; ++q) {
+                        uint4* pp = reinterpret_cast<uint4*>(row + ((q ^ ((lane >> 1) & 3)) << 4));
+                        float cv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                        if (use_c) {
+                            const uint4 in = *pp;
+                            const uint32_t iw[4] = {in.x, in.y, in.z, in.w};
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                const float2 f = bf16 ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&iw[t]))
+                                                      : __half22float2(*reinterpret_cast<const __half2*>(&iw[t]));
+                                cv[2 * t] = f.x;
+                                cv[2 * t + 1] = f.y;
+                            }
+                        }
+                        uint32_t ow[4];
 #pragma unroll
                         for (int t = 0; t < 4; ++t) {
-                            const float2 f = bf16 ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&iw[t]))
-                                                  : __half22float2(*reinterpret_cast<const __half2*>(&iw[t]));
-                            cv[2 * t] = f.x;
-                            cv[2 * t + 1] = f.y;
+                            const float a = epi_value<F>(e, v[8 * q + 2 * t], cv[2 * t], bcol(8 * q + 2 * t));
+                            const float b2 = epi_value<F>(e, v[8 * q + 2 * t + 1], cv[2 * t + 1], bcol(8 * q + 2 * t + 1));
+                            if (bf16) {
+                                __nv_bfloat162 h = __floats2bfloat162_rn(a, b2);
+                                ow[t] = *reinterpret_cast<uint32_t*>(&h);
+                            } else {
+                                __half2 h = __floats2half2_rn(a, b2);
+                                ow[t] = *reinterpret_cast<uint32_t*>(&h);
+                            }
                         }
+                        *pp = make_uint4(ow[0], ow[1], ow[2], ow[3]);
                     }
-                    uint32_t ow[4];
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const float a = epi_value(e, v[8 * q + 2 * t], cv[2 * t]);
-                        const float b2 = epi_value(e, v[8 * q + 2 * t + 1], cv[2 * t + 1]);
-                        if (bf16) {
-                            __nv_bfloat162 h = __floats2bfloat162_rn(a, b2);
-                            ow[t] = *reinterpret_cast<uint32_t*>(&h);
-                        } else {
-                            __half2 h = __floats2half2_rn(a, b2);
-                            ow[t] = *reinterpret_cast<uint32_t*>(&h);
-                        }
-                    }
-                    *pp = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-                }
+                };
+                with_epi_act(e, put);
             }
             fence_proxy_async_smem();
         }
@@ -668,6 +770,7 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
     Unit u;
     uint32_t acc_it = 0;
     while (ok && next_unit(P, w, u, BN)) {
+        if (e.flags) prefetch_bias(e, u.y_row0, BN, lane);
         const int buf = acc_it & 1;
         const uint32_t aph = (acc_it >> 1) & 1;
         ++acc_it;

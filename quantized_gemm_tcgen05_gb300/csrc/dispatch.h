@@ -30,6 +30,7 @@ struct Problem {
     const void* C; int64_t ldc, c_bs;
     void* D; int64_t ldd, d_bs;
     float alpha, beta;
+    int32_t epi_flags, bias_type; const void* bias;   // fused bias / activation
     // grouped
     const int32_t* offsets; int32_t num_experts;
 };

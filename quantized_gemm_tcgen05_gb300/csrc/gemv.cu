@@ -233,7 +233,13 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, MT == 1 ? 4 : 2) gemv_kernel(
                                                    ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.C)[ci])
                                                    : __half2float(reinterpret_cast<const __half*>(p.C)[ci]));
                 }
-                const float d = fmaf(p.alpha, sum, p.beta * cv);
+                float d = fmaf(p.alpha, sum, p.beta * cv);
+                if (p.epi_flags) {
+                    // the fused steps of the tensor-core epilogue, same order
+                    if (p.epi_flags & EPI_BIAS) d += ld_elem(p.bias, p.bias_type, n);
+                    if (p.epi_flags & EPI_RELU) d = d < 0.0f ? 0.0f : d;
+                    if (p.epi_flags & EPI_GELU) d = 0.5f * d * (1.0f + erff(d * 0.70710678118654752f));
+                }
                 const int64_t di = (int64_t)m * p.ldd + n;
                 if (p.d_type == DT_F32)
                     reinterpret_cast<float*>(p.D)[di] = d;

@@ -30,6 +30,9 @@ struct GemvParams {
     int32_t gb;      // group size of V along K
     int32_t d_type;  // DT_F32 / DT_F16 / DT_BF16
     int32_t kslices; // warps that split one row group's K range (1, 2, 4 or 8)
+    int32_t epi_flags;  // EPI_BIAS | EPI_RELU | EPI_GELU, applied after alpha / beta
+    int32_t bias_type;  // DT_F32 / DT_F16 / DT_BF16
+    const void* bias;   // N values, one per output column
 };
 
 // Launch for M <= GEMV_MAX_M.  Returns cudaErrorInvalidValue for shapes the

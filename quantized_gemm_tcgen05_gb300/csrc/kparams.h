@@ -38,7 +38,14 @@ struct EpiParams {
     int32_t vec_ok;    // C/D bases and ld allow 16-byte vector access
     int32_t tma;       // C/D move through shared memory with TMA (tmC / tmD)
     int32_t ncb;       // shared-memory C/D buffers per epilogue warp (TMA path)
+    int32_t flags;     // EPI_BIAS | EPI_RELU | EPI_GELU (the ABI's GEMM_EPILOGUE_*)
+    int32_t bias_type; // DT_F32 / DT_F16 / DT_BF16
+    const void* bias;  // N values, one per output column (EPI_BIAS)
 };
+
+// Fused epilogue steps after x = alpha * acc + beta * c: + bias[column], then
+// ReLU or GELU (DeepGEMM kernel-set blog, section 6.1).
+enum EpiFlags : int32_t { EPI_BIAS = 1, EPI_RELU = 2, EPI_GELU = 4 };
 
 // Group-wise scaling / int4 dequantisation of one shared-memory operand
 // before the tensor core reads it (the role of the scale operands U/V that

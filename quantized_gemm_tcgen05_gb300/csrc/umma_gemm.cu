@@ -7,7 +7,8 @@ namespace qg {
 
 __device__ uint32_t g_device_status[4];
 
-// D = beta * C (or 0) for K == 0, where no accumulator exists.
+// D = beta * C (or 0), then the fused bias / activation, for K == 0, where
+// no accumulator exists.
 __global__ void scale_c_kernel(EpiParams e, int64_t batches) {
     const int64_t total = batches * e.M * e.N;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
@@ -15,7 +16,8 @@ __global__ void scale_c_kernel(EpiParams e, int64_t batches) {
         const int64_t b = i / (e.M * e.N), rem = i % (e.M * e.N);
         const int64_t m = rem / e.N, n = rem % e.N;
         const float c = e.beta != 0.0f ? ld_elem(e.C, e.d_type, b * e.c_bstride + m * e.ldc + n) : 0.0f;
-        st_elem(e.D, e.d_type, b * e.d_bstride + m * e.ldd + n, e.beta != 0.0f ? e.beta * c : 0.0f);
+        const float x = e.beta != 0.0f ? e.beta * c : 0.0f;
+        st_elem(e.D, e.d_type, b * e.d_bstride + m * e.ldd + n, e.flags ? epi_finish(e, x, bias_at(e, n)) : x);
     }
 }
 

@@ -1,0 +1,8 @@
+// Instantiation of the dense tcgen05 GEMM kernel for tile width 64 (one
+// width per translation unit, so they compile in parallel).
+#include "umma_gemm.cuh"
+
+namespace qg {
+template cudaError_t launch_umma_bn<64>(const GemmMaps&, const GemmKernelParams&, int, cudaStream_t);
+template int umma_stages_bn<64>(int);
+}  // namespace qg

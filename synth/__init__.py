@@ -82,6 +82,9 @@ class Problem:
     u_type: int | None = None
     ga: int = 0
     name: str = ""
+    epilogue: int = 0                # fused epilogue flags: 1 bias, 2 ReLU, 4 GELU
+    bias: np.ndarray | None = None   # [N] storage bits (float32 values for F32)
+    bias_type: int | None = None
 
 
 def _rng(seed: int) -> np.random.Generator:
@@ -167,6 +170,9 @@ class GroupedProblem:
     alpha: float = 1.0
     beta: float = 0.0
     name: str = ""
+    epilogue: int = 0
+    bias: np.ndarray | None = None
+    bias_type: int | None = None
 
 
 def grouped(counts, N, K, *, seed, a_type=BF16, d_type=BF16, a_scale=1.0, b_scale=0.02,
@@ -193,3 +199,13 @@ def batched(batch, M, N, K, *, seed, a_type=BF16, d_type=BF16, name="") -> Group
     """Uniform batch: every 'expert' gets M rows (offsets are multiples of M)."""
     return grouped([M] * batch, N, K, seed=seed, a_type=a_type, d_type=d_type, a_scale=1.0,
                    b_scale=1.0 / np.sqrt(K), name=name or f"batched {batch}x{M}x{N}x{K}")
+
+
+def with_epilogue(p, epilogue, *, seed, bias_type=F32, scale=1.0):
+    """Set fused-epilogue flags on a problem; with the bias flag, draw a bias
+    of N(0, scale^2) values per output column, stored as bias_type."""
+    p.epilogue = epilogue
+    if epilogue & 1:
+        b = _rng(seed).standard_normal(size=p.N, dtype=np.float32) * np.float32(scale)
+        p.bias, p.bias_type = _round_bits(b, bias_type), bias_type
+    return p

@@ -98,11 +98,27 @@ def run_problem(lib, p, o=None, D=None, C=None, stream=None, workspace=True):
     if p.V is not None:
         V, ldv = padded_rows(p.V, p.v_type)
         Vd = qg.layout(p.v_type, qg.GEMM_ROW_MAJOR, p.K // p.gb, p.N, ldv)
+    bias = _attach_epilogue(p, o)
     st = stream if stream is not None else qg.current_stream()
     rc = qg.gemm_run(lib.h, o, p.alpha, qg.ptr(A), Ad, qg.ptr(U), Ud, qg.ptr(B), Bd, qg.ptr(V), Vd, p.beta,
                      qg.ptr(C), Cd, qg.ptr(D), Dd, lib.ws.c if workspace else None, st)
     torch.cuda.synchronize()
+    del bias
     return rc, D
+
+
+def _attach_epilogue(p, o):
+    """Copy the problem's fused-epilogue flags and bias (if any) into the op.
+    Returns the device bias tensor, which must outlive the call."""
+    flags = getattr(p, "epilogue", 0) or 0
+    if not flags:
+        return None
+    o.epilogue = flags
+    if not flags & qg.GEMM_EPILOGUE_BIAS:
+        return None
+    bias = dev_bits(p.bias, p.bias_type)
+    o.bias, o.bias_type = qg.ptr(bias), p.bias_type
+    return bias
 
 
 def grouped_to_device(gp):
@@ -117,10 +133,13 @@ def run_grouped(lib, gp, o=None, A=None, B=None, off=None):
         A, B, off = grouped_to_device(gp)
     T = int(gp.offsets[-1])
     D = torch.full((T, gp.N), float("nan"), dtype=TORCH_DT[gp.d_type], device="cuda")
-    rc = qg.gemm_run_grouped(lib.h, o or op(), gp.alpha, qg.ptr(A), qg.row_major(A), None, None, qg.ptr(B),
+    o = o or op()
+    bias = _attach_epilogue(gp, o)
+    rc = qg.gemm_run_grouped(lib.h, o, gp.alpha, qg.ptr(A), qg.row_major(A), None, None, qg.ptr(B),
                              qg.col_major_from_nk(B), None, None, gp.beta, None, None, qg.ptr(D), qg.row_major(D),
                              qg.ptr(off), len(gp.counts), lib.ws.c, qg.current_stream())
     torch.cuda.synchronize()
+    del bias
     return rc, D
 
 

@@ -188,6 +188,54 @@ def test_beta_zero_does_not_read_c():
     assert np.isfinite(ref).all()
 
 
+# Standard normal CDF at 1, 2 and sqrt(2) (printed in every normal table).
+PHI_1, PHI_2, PHI_SQRT2 = 0.8413447460685429, 0.9772498680518208, 0.9213503964748575
+
+
+def _scalar_problem(x_bits, dtype=BF16):
+    """A 1 x 3 x 1 product whose three outputs are the values x_bits decode to."""
+    one = 0x3F80 if dtype == BF16 else 0x3C00
+    p = synth.dense(1, len(x_bits), 1, seed=0, a_type=dtype, d_type=F32)
+    p.A = np.array([[one]], dtype=np.uint16)
+    p.B = np.array([[b] for b in x_bits], dtype=np.uint16)
+    return p
+
+
+def test_gelu_closed_forms():
+    # GELU(x) = x * Phi(x): x = 1, 2, -1 (bf16 0x3F80, 0x4000, 0xBF80)
+    p = synth.with_epilogue(_scalar_problem([0x3F80, 0x4000, 0xBF80]), 4, seed=0)
+    ref, bound = oracle.gemm(p)
+    assert ref[0] == pytest.approx([PHI_1, 2 * PHI_2, -(1 - PHI_1)], rel=1e-15, abs=1e-16)
+    assert np.array_equal(bound[0], 1.129 * np.array([1.0, 2.0, 1.0]))
+    # the bound's factor covers the largest slope of x * Phi(x), at x = sqrt 2
+    phi = math.exp(-1.0) / math.sqrt(2 * math.pi)
+    assert PHI_SQRT2 + math.sqrt(2) * phi < 1.129
+
+
+def test_relu_bias_order_and_nan():
+    # x = -1 (+ bias 2 before the activation gives 1; ReLU first would give 2),
+    # x = 3 with bias 2 -> 5; a NaN input stays NaN
+    p = synth.with_epilogue(_scalar_problem([0xBF80, 0x4040, 0x7FC0]), 1 | 2, seed=0)
+    p.bias, p.bias_type = np.array([2.0, 2.0, 0.0], dtype=np.float32), F32
+    ref, bound = oracle.gemm(p)
+    assert ref[0][0] == 1.0 and ref[0][1] == 5.0 and math.isnan(ref[0][2])
+    assert bound[0][0] == 3.0 and bound[0][1] == 5.0
+    p.epilogue = 2
+    ref, _ = oracle.gemm(p)
+    assert ref[0][0] == 0.0 and ref[0][1] == 3.0
+
+
+def test_bias_follows_alpha_and_beta():
+    # D = act(alpha * acc + beta * c + bias_j); bias broadcast over rows, by column
+    p = synth.dense(4, 3, 8, seed=31, a_type=F16, d_type=F16, alpha=1.5, beta=-0.5)
+    ref0, b0 = oracle.gemm(p)
+    synth.with_epilogue(p, 1, seed=32, bias_type=BF16)
+    ref1, b1 = oracle.gemm(p)
+    bias = lib_decode(BF16, p.bias)
+    assert np.array_equal(ref1, ref0 + bias[None, :])
+    assert np.array_equal(b1, b0 + np.abs(bias)[None, :])
+
+
 def test_entries_agree_with_full():
     p = synth.dense(37, 29, 40, seed=21, a_type=BF16, d_type=BF16, alpha=1.5, beta=0.5)
     ref, bound = oracle.gemm(p)
