@@ -51,7 +51,7 @@ typedef enum {
 } gemm_status_t;
 
 /* ---- operand description ------------------------------------------------------ */
-typedef enum { GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2, GEMM_S4 = 3 } gemm_dtype_t;
+typedef enum { GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2, GEMM_S4 = 3, GEMM_S8 = 4 } gemm_dtype_t;
 typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_order_t;
 
 /*
@@ -111,6 +111,17 @@ enum {
 };
 
 /*
+ * Output quantisation (DeepGEMM kernel-set blog, section 6.2): a D of type
+ * GEMM_S8 receives y = round(x * out_scale[i] + zp) for row i, where x is the
+ * fp32 value the epilogue would otherwise round to D (after alpha/beta and the
+ * fused bias / activation).  The product-plus-offset is one fp32 fma, the
+ * rounding is to nearest-even and the result saturates to [-128, 127] (NaN
+ * gives 0).  It
+ * needs beta == 0 (C is not read) and one batch; grouped problems index the
+ * scales by D's row (token).
+ */
+
+/*
  * Operation: "dispatch policy, epilogue, quantization config" (Gemm Interface,
  * I/O Contract).
  */
@@ -125,6 +136,9 @@ typedef struct {
                               aligned to their element size, owned by the caller;
                               ignored otherwise                                       */
     int32_t bias_type;     /* GEMM_F32 / GEMM_F16 / GEMM_BF16                         */
+    int32_t out_zero_point;/* GEMM_S8 D: the zero point zp                           */
+    const float* out_scale;/* GEMM_S8 D: M fp32 scales on the device, one per row of D
+                              (per token); ignored for other D types                  */
 } gemm_op_t;
 
 /*

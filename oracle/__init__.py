@@ -203,6 +203,16 @@ def gemm_entries(p, ii, jj):
     return ref, bound
 
 
+def quantize_s8(x, scale, zp):
+    """Output quantisation (DeepGEMM kernel-set blog, section 6.2): the int8 code
+    round(x * scale_i + zp) of every value of row i, to nearest-even, saturated
+    to [-128, 127], NaN giving 0.  x: [M, N] values before rounding (float64),
+    scale: [M] per-row (per-token) scales."""
+    t = np.asarray(x, dtype=np.float64) * np.asarray(scale, dtype=np.float64)[:, None] + float(zp)
+    q = np.clip(np.rint(t), -128, 127)
+    return np.where(np.isnan(t), 0.0, q)
+
+
 class _Slice:
     """One expert's rows of a grouped problem, viewed as a dense problem."""
 

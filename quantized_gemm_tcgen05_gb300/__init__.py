@@ -26,7 +26,7 @@ GEMM_ERR_NO_KERNEL = 5
 GEMM_ERR_DEVICE_TIMEOUT = 6
 GEMM_ERR_BAD_CACHE = 7
 
-GEMM_F32, GEMM_F16, GEMM_BF16, GEMM_S4 = 0, 1, 2, 3
+GEMM_F32, GEMM_F16, GEMM_BF16, GEMM_S4, GEMM_S8 = 0, 1, 2, 3, 4
 GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
 GEMM_DISPATCH_DEFAULT, GEMM_DISPATCH_MEASURE, GEMM_DISPATCH_REUSE = 0, 1, 2
 GEMM_EPILOGUE_DEFAULT, GEMM_EPILOGUE_BIAS, GEMM_EPILOGUE_RELU, GEMM_EPILOGUE_GELU = 0, 1, 2, 4
@@ -63,7 +63,8 @@ class gemm_layout_t(ctypes.Structure):
 class gemm_op_t(ctypes.Structure):
     _fields_ = [("dispatch", ctypes.c_int32), ("epilogue", ctypes.c_int32), ("quant_a_group", ctypes.c_int32),
                 ("quant_b_group", ctypes.c_int32), ("splitk", ctypes.c_int32), ("streamk", ctypes.c_int32),
-                ("bias", ctypes.c_void_p), ("bias_type", ctypes.c_int32)]
+                ("bias", ctypes.c_void_p), ("bias_type", ctypes.c_int32), ("out_zero_point", ctypes.c_int32),
+                ("out_scale", ctypes.c_void_p)]
 
 
 class gemm_workspace_t(ctypes.Structure):
@@ -226,7 +227,7 @@ def gemm_grouped_block(sizes, block_m, block):
 
 def _dtype_code(t):
     import torch
-    return {torch.float32: GEMM_F32, torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16}[t]
+    return {torch.float32: GEMM_F32, torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16, torch.int8: GEMM_S8}[t]
 
 
 def layout(type_, order, rows, cols, ld, num=1, batch_stride=0):

@@ -54,7 +54,8 @@ namespace {
 
 bool is16(int32_t t) { return t == GEMM_F16 || t == GEMM_BF16; }
 bool is_float_out(int32_t t) { return t == GEMM_F32 || t == GEMM_F16 || t == GEMM_BF16; }
-static_assert(GEMM_F32 == DT_F32 && GEMM_F16 == DT_F16 && GEMM_BF16 == DT_BF16 && GEMM_S4 == DT_S4,
+static_assert(GEMM_F32 == DT_F32 && GEMM_F16 == DT_F16 && GEMM_BF16 == DT_BF16 && GEMM_S4 == DT_S4 &&
+                  GEMM_S8 == DT_S8,
               "the C ABI's dtype codes are the kernels' codes");
 static_assert(GEMM_EPILOGUE_BIAS == EPI_BIAS && GEMM_EPILOGUE_RELU == EPI_RELU && GEMM_EPILOGUE_GELU == EPI_GELU,
               "the C ABI's epilogue flags are the kernels' flags");
@@ -343,6 +344,8 @@ int launch_gemv_choice(gemm_handle* h, const Problem& p, cudaStream_t st) {
     g.epi_flags = p.epi_flags;
     g.bias = p.bias;
     g.bias_type = p.bias_type;
+    g.qscale = p.qscale;
+    g.qzp = p.qzp;
     // enough warps for the weight stream: about 24 per SM (GEMM_GEMV_KSLICES
     // = 1, 2, 4 or 8 overrides the split, for tuning)
     g.kslices = gemv_kslices(p.N, p.K, g.b_int4, (int64_t)h->sm_count * 24);
@@ -385,8 +388,10 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
     e.flags = p.epi_flags;
     e.bias = p.bias;
     e.bias_type = p.bias_type;
+    e.qscale = p.qscale;
+    e.qzp = p.qzp;
     e.swap = c.swap;
-    const int64_t eb = p.d_type == GEMM_F32 ? 4 : 2;
+    const int64_t eb = p.d_type == GEMM_F32 ? 4 : (p.d_type == GEMM_S8 ? 1 : 2);
     e.vec_ok = aligned16(p.D) && (p.ldd * eb) % 16 == 0 &&
                (e.C == nullptr || (aligned16(p.C) && (p.ldc * eb) % 16 == 0)) &&
                (p.batches == 1 || ((p.d_bs * eb) % 16 == 0 && (e.C == nullptr || (p.c_bs * eb) % 16 == 0)));
@@ -456,7 +461,8 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
         };
         const char* et = getenv("GEMM_EPI_TMA");
         const bool allowed = !(et && et[0] == '0');
-        e.tma = allowed && !c.swap && p.family != FAM_GROUPED && c.bn >= 32 && ok16(p.D, p.ldd, p.d_bs) &&
+        e.tma = allowed && !c.swap && p.family != FAM_GROUPED && c.bn >= 32 && p.d_type != GEMM_S8 &&
+                ok16(p.D, p.ldd, p.d_bs) &&
                 (e.C == nullptr || ok16(p.C, p.ldc, p.c_bs)) && !(c.pair && es == 4);
         if (e.tma) {
             // buffers per epilogue warp: 32 KB of epilogue shared memory (16 KB
@@ -620,6 +626,8 @@ int dispatch_and_run(gemm_handle* h, const gemm_op_t* op, Problem& p, const gemm
         e.flags = p.epi_flags;
         e.bias = p.bias;
         e.bias_type = p.bias_type;
+        e.qscale = p.qscale;
+        e.qzp = p.qzp;
         h->last_choice = "scale_c";
         return launch_scale_c(e, p.batches, st) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
@@ -720,7 +728,7 @@ int build_problem(gemm_handle* h, const gemm_op_t* op, float alpha, const void* 
     p.d_type = Ddesc->type;
     if (!is16(p.a_type)) return GEMM_ERR_UNSUPPORTED;
     if (!(p.b_type == p.a_type || p.b_type == GEMM_S4)) return GEMM_ERR_UNSUPPORTED;
-    if (!is_float_out(p.d_type)) return GEMM_ERR_UNSUPPORTED;
+    if (!is_float_out(p.d_type) && p.d_type != GEMM_S8) return GEMM_ERR_UNSUPPORTED;
     int rc;
     if ((rc = check_layout(Adesc, GEMM_ROW_MAJOR, p.M, p.K))) return rc;
     if ((rc = check_layout(Bdesc, GEMM_COL_MAJOR, p.K, p.N))) return rc;
@@ -728,6 +736,14 @@ int build_problem(gemm_handle* h, const gemm_op_t* op, float alpha, const void* 
     p.alpha = alpha;
     p.beta = beta;
     p.epi_flags = op->epilogue;
+    if (p.d_type == GEMM_S8) {
+        // output quantisation: per-row fp32 scales on the device; C is not read
+        if (beta != 0.0f || Ddesc->num != 1) return GEMM_ERR_UNSUPPORTED;
+        if (!op->out_scale || (reinterpret_cast<uintptr_t>(op->out_scale) & 3)) return GEMM_ERR_INVALID_ARG;
+        if (p.M > 0 && !device_pointer(h, op->out_scale)) return GEMM_ERR_INVALID_ARG;
+        p.qscale = op->out_scale;
+        p.qzp = op->out_zero_point;
+    }
     p.bias = (op->epilogue & GEMM_EPILOGUE_BIAS) ? op->bias : nullptr;
     p.bias_type = op->bias_type;
     p.A = A;

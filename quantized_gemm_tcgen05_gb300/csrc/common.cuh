@@ -151,6 +151,14 @@ __device__ __forceinline__ void st_elem(void* p, int32_t t, int64_t i, float x) 
         static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(x);
 }
 
+// Output quantisation for an int8 D (DeepGEMM kernel-set blog, section 6.2):
+// round(x * scale + zp) with one fp32 fma, nearest-even, saturated to int8
+// (a NaN becomes 0, as the conversion defines).
+__device__ __forceinline__ int32_t quant_s8(float x, float scale, int32_t zp) {
+    const int32_t q = __float2int_rn(fmaf(x, scale, (float)zp));
+    return q < -128 ? -128 : (q > 127 ? 127 : q);
+}
+
 // Four consecutive elements, 16-byte (f32) or 8-byte (16-bit) aligned.
 __device__ __forceinline__ float4 ld4(const void* p, int32_t t, int64_t i) {
     if (t == DT_F32) return *reinterpret_cast<const float4*>(static_cast<const float*>(p) + i);
@@ -191,6 +199,28 @@ __device__ __forceinline__ void st4(void* p, int32_t t, int64_t i, float4 v) {
 // column and chunk, not per element.
 __device__ __forceinline__ float bias_at(const EpiParams& e, int64_t n) {
     return ((e.flags & EPI_BIAS) && n < e.N) ? ld_elem(e.bias, e.bias_type, n) : 0.0f;
+}
+
+// Store one output value of row m at element index i: rounded to D's type, or
+// quantised with the row's scale for an int8 D.
+__device__ __forceinline__ void store_out(const EpiParams& e, int64_t i, float x, int64_t m) {
+    if (e.d_type == DT_S8)
+        static_cast<int8_t*>(e.D)[i] = (int8_t)quant_s8(x, e.qscale[m], e.qzp);
+    else
+        st_elem(e.D, e.d_type, i, x);
+}
+
+// Four consecutive values of row m (aligned as st4 needs; 4 bytes for int8).
+__device__ __forceinline__ void store_out4(const EpiParams& e, int64_t i, float4 v, int64_t m) {
+    if (e.d_type == DT_S8) {
+        const float s = e.qscale[m];
+        const uint32_t b = (uint32_t)(quant_s8(v.x, s, e.qzp) & 0xFF) | ((uint32_t)(quant_s8(v.y, s, e.qzp) & 0xFF) << 8) |
+                           ((uint32_t)(quant_s8(v.z, s, e.qzp) & 0xFF) << 16) |
+                           ((uint32_t)(quant_s8(v.w, s, e.qzp) & 0xFF) << 24);
+        *reinterpret_cast<uint32_t*>(static_cast<int8_t*>(e.D) + i) = b;
+    } else {
+        st4(e.D, e.d_type, i, v);
+    }
 }
 
 // Bring the bias of a unit's output columns into L1 before its accumulator is
@@ -347,7 +377,7 @@ __device__ __forceinline__ void store_chunk_t(const EpiParams& e, const Unit& u,
 #pragma unroll
         for (int j = 0; j < W; ++j) {
             const int64_t m = u.y_row0 + col0 + j;
-            if (m < e.M) st_elem(e.D, e.d_type, boff_d + m * e.ldd + n, epi_value<ACT>(e, v[j], cc.v[j], bn));
+            if (m < e.M) store_out(e, boff_d + m * e.ldd + n, epi_value<ACT>(e, v[j], cc.v[j], bn), m);
         }
         return;
     }
@@ -378,10 +408,10 @@ __device__ __forceinline__ void store_chunk_t(const EpiParams& e, const Unit& u,
                                      epi_value<ACT>(e, a.z, cc.v[4 * it + 2], bq[2]),
                                      epi_value<ACT>(e, a.w, cc.v[4 * it + 3], bq[3]));
         if (e.vec_ok && n0 + 3 < e.N) {
-            st4(e.D, e.d_type, di, o);
+            store_out4(e, di, o, m);
         } else {
             const float ov[4] = {o.x, o.y, o.z, o.w};
-            for (int q = 0; q < 4 && n0 + q < e.N; ++q) st_elem(e.D, e.d_type, di + q, ov[q]);
+            for (int q = 0; q < 4 && n0 + q < e.N; ++q) store_out(e, di + q, ov[q], m);
         }
     }
     __syncwarp();

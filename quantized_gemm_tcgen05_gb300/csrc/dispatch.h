@@ -31,6 +31,7 @@ struct Problem {
     void* D; int64_t ldd, d_bs;
     float alpha, beta;
     int32_t epi_flags, bias_type; const void* bias;   // fused bias / activation
+    const float* qscale; int32_t qzp;                 // int8 D: per-row scale, zero point
     // grouped
     const int32_t* offsets; int32_t num_experts;
 };

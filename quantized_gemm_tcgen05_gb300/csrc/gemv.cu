@@ -241,7 +241,9 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, MT == 1 ? 4 : 2) gemv_kernel(
                     if (p.epi_flags & EPI_GELU) d = 0.5f * d * (1.0f + erff(d * 0.70710678118654752f));
                 }
                 const int64_t di = (int64_t)m * p.ldd + n;
-                if (p.d_type == DT_F32)
+                if (p.d_type == DT_S8)
+                    reinterpret_cast<int8_t*>(p.D)[di] = (int8_t)quant_s8(d, p.qscale[m], p.qzp);
+                else if (p.d_type == DT_F32)
                     reinterpret_cast<float*>(p.D)[di] = d;
                 else if (p.d_type == DT_BF16)
                     reinterpret_cast<__nv_bfloat16*>(p.D)[di] = __float2bfloat16_rn(d);

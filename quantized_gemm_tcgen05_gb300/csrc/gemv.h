@@ -33,6 +33,8 @@ struct GemvParams {
     int32_t epi_flags;  // EPI_BIAS | EPI_RELU | EPI_GELU, applied after alpha / beta
     int32_t bias_type;  // DT_F32 / DT_F16 / DT_BF16
     const void* bias;   // N values, one per output column
+    const float* qscale;  // d_type DT_S8: M scales, one per output row
+    int32_t qzp;          // d_type DT_S8: zero point
 };
 
 // Launch for M <= GEMV_MAX_M.  Returns cudaErrorInvalidValue for shapes the

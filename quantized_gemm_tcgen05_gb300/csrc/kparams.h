@@ -10,7 +10,7 @@
 
 namespace qg {
 
-enum DType : int32_t { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2, DT_S4 = 3 };
+enum DType : int32_t { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2, DT_S4 = 3, DT_S8 = 4 };
 
 // Where a bounded wait gave up (recorded in the device status word).
 enum WaitSite : uint32_t {
@@ -33,7 +33,7 @@ struct EpiParams {
     int64_t d_bstride, c_bstride;  // elements between batches (0 for grouped)
     int64_t M, N;      // output rows / columns (per batch)
     float alpha, beta;
-    int32_t d_type;    // DT_F32 / DT_F16 / DT_BF16 (C has the same type)
+    int32_t d_type;    // DT_F32 / DT_F16 / DT_BF16 (C has the same type), or DT_S8 (quantised, no C)
     int32_t swap;      // 0: tile rows are D rows; 1: tile rows are D columns
     int32_t vec_ok;    // C/D bases and ld allow 16-byte vector access
     int32_t tma;       // C/D move through shared memory with TMA (tmC / tmD)
@@ -41,6 +41,8 @@ struct EpiParams {
     int32_t flags;     // EPI_BIAS | EPI_RELU | EPI_GELU (the ABI's GEMM_EPILOGUE_*)
     int32_t bias_type; // DT_F32 / DT_F16 / DT_BF16
     const void* bias;  // N values, one per output column (EPI_BIAS)
+    const float* qscale;  // d_type DT_S8: M scales, one per output row
+    int32_t qzp;          // d_type DT_S8: zero point
 };
 
 // Fused epilogue steps after x = alpha * acc + beta * c: + bias[column], then

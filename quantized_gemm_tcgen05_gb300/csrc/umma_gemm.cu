@@ -17,7 +17,7 @@ __global__ void scale_c_kernel(EpiParams e, int64_t batches) {
         const int64_t m = rem / e.N, n = rem % e.N;
         const float c = e.beta != 0.0f ? ld_elem(e.C, e.d_type, b * e.c_bstride + m * e.ldc + n) : 0.0f;
         const float x = e.beta != 0.0f ? e.beta * c : 0.0f;
-        st_elem(e.D, e.d_type, b * e.d_bstride + m * e.ldd + n, e.flags ? epi_finish(e, x, bias_at(e, n)) : x);
+        store_out(e, b * e.d_bstride + m * e.ldd + n, e.flags ? epi_finish(e, x, bias_at(e, n)) : x, m);
     }
 }
 

@@ -26,7 +26,7 @@ from __future__ import annotations
 import dataclasses
 import numpy as np
 
-F32, F16, BF16, S4 = 0, 1, 2, 3
+F32, F16, BF16, S4, S8 = 0, 1, 2, 3, 4
 DTYPE_NAMES = {F32: "f32", F16: "f16", BF16: "bf16", S4: "s4"}
 
 
@@ -85,6 +85,8 @@ class Problem:
     epilogue: int = 0                # fused epilogue flags: 1 bias, 2 ReLU, 4 GELU
     bias: np.ndarray | None = None   # [N] storage bits (float32 values for F32)
     bias_type: int | None = None
+    q_scale: np.ndarray | None = None  # int8 D: [M] float32 per-row scales
+    q_zp: int = 0                      # int8 D: zero point
 
 
 def _rng(seed: int) -> np.random.Generator:
@@ -173,6 +175,8 @@ class GroupedProblem:
     epilogue: int = 0
     bias: np.ndarray | None = None
     bias_type: int | None = None
+    q_scale: np.ndarray | None = None
+    q_zp: int = 0
 
 
 def grouped(counts, N, K, *, seed, a_type=BF16, d_type=BF16, a_scale=1.0, b_scale=0.02,
@@ -208,4 +212,12 @@ def with_epilogue(p, epilogue, *, seed, bias_type=F32, scale=1.0):
     if epilogue & 1:
         b = _rng(seed).standard_normal(size=p.N, dtype=np.float32) * np.float32(scale)
         p.bias, p.bias_type = _round_bits(b, bias_type), bias_type
+    return p
+
+
+def with_out_quant(p, scales, zp=0):
+    """Make D an int8 output with per-row (per-token) scales and a zero point."""
+    p.d_type = S8
+    p.q_scale = np.ascontiguousarray(scales, dtype=np.float32)
+    p.q_zp = int(zp)
     return p

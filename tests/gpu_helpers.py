@@ -19,7 +19,7 @@ import quantized_gemm_tcgen05_gb300 as qg
 import oracle
 import synth
 
-TORCH_DT = {synth.F32: torch.float32, synth.F16: torch.float16, synth.BF16: torch.bfloat16}
+TORCH_DT = {synth.F32: torch.float32, synth.F16: torch.float16, synth.BF16: torch.bfloat16, synth.S8: torch.int8}
 
 
 def dev_bits(bits, dtype):
@@ -47,6 +47,27 @@ def tolerance(ref, bound, d_type):
     if d_type != synth.F32:
         tol = tol + oracle.ulp(d_type, ref)
     return tol
+
+
+def assert_quant(d, ref, bound, scale, zp, what=""):
+    """An int8 D against the oracle's pre-rounding values: each code must lie
+    between the codes of ref*scale+zp moved by the fp32 value's tolerance (and
+    the fma's rounding) either way; where no rounding boundary lies within
+    that band this is the single exact code."""
+    d = np.asarray(d, dtype=np.float64)
+    s = np.asarray(scale, dtype=np.float64)[:, None]
+    band = tolerance(ref, bound, synth.F32) * np.abs(s) + 1e-4
+    lo = oracle.quantize_s8(ref - band / np.abs(s) * np.sign(s), scale, zp)
+    hi = oracle.quantize_s8(ref + band / np.abs(s) * np.sign(s), scale, zp)
+    lo, hi = np.minimum(lo, hi), np.maximum(lo, hi)
+    bad = (d < lo) | (d > hi)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        exact = oracle.quantize_s8(ref, scale, zp)
+        msg = ", ".join(f"{tuple(i)}: got {d[tuple(i)]:.0f} want {exact[tuple(i)]:.0f} [{lo[tuple(i)]:.0f}, {hi[tuple(i)]:.0f}]"
+                        for i in idx)
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} int8 codes out of range; {msg}")
+    return int((lo != hi).sum())
 
 
 def assert_close(d, ref, bound, d_type, what=""):
@@ -84,7 +105,8 @@ def run_problem(lib, p, o=None, D=None, C=None, stream=None, workspace=True):
     Ad = qg.row_major(A)
     Bd = qg.col_major_from_nk(B, k=p.K, type_=p.b_type)
     if D is None:
-        D = torch.full((p.M, p.N), float("nan"), dtype=TORCH_DT[p.d_type], device="cuda")
+        fill = 101 if p.d_type == synth.S8 else float("nan")  # a code the tests' scales never produce
+        D = torch.full((p.M, p.N), fill, dtype=TORCH_DT[p.d_type], device="cuda")
     Dd = qg.row_major(D)
     Cd = None
     if p.beta != 0.0 and C is None:
@@ -99,11 +121,15 @@ def run_problem(lib, p, o=None, D=None, C=None, stream=None, workspace=True):
         V, ldv = padded_rows(p.V, p.v_type)
         Vd = qg.layout(p.v_type, qg.GEMM_ROW_MAJOR, p.K // p.gb, p.N, ldv)
     bias = _attach_epilogue(p, o)
+    qs = None
+    if p.d_type == synth.S8:
+        qs = torch.from_numpy(np.ascontiguousarray(p.q_scale, dtype=np.float32)).cuda()
+        o.out_scale, o.out_zero_point = qg.ptr(qs), p.q_zp
     st = stream if stream is not None else qg.current_stream()
     rc = qg.gemm_run(lib.h, o, p.alpha, qg.ptr(A), Ad, qg.ptr(U), Ud, qg.ptr(B), Bd, qg.ptr(V), Vd, p.beta,
                      qg.ptr(C), Cd, qg.ptr(D), Dd, lib.ws.c if workspace else None, st)
     torch.cuda.synchronize()
-    del bias
+    del bias, qs
     return rc, D
 
 
@@ -132,14 +158,19 @@ def run_grouped(lib, gp, o=None, A=None, B=None, off=None):
     if A is None:
         A, B, off = grouped_to_device(gp)
     T = int(gp.offsets[-1])
-    D = torch.full((T, gp.N), float("nan"), dtype=TORCH_DT[gp.d_type], device="cuda")
+    fill = 101 if gp.d_type == synth.S8 else float("nan")
+    D = torch.full((T, gp.N), fill, dtype=TORCH_DT[gp.d_type], device="cuda")
     o = o or op()
     bias = _attach_epilogue(gp, o)
+    qs = None
+    if gp.d_type == synth.S8:
+        qs = torch.from_numpy(np.ascontiguousarray(gp.q_scale, dtype=np.float32)).cuda()
+        o.out_scale, o.out_zero_point = qg.ptr(qs), gp.q_zp
     rc = qg.gemm_run_grouped(lib.h, o, gp.alpha, qg.ptr(A), qg.row_major(A), None, None, qg.ptr(B),
                              qg.col_major_from_nk(B), None, None, gp.beta, None, None, qg.ptr(D), qg.row_major(D),
                              qg.ptr(off), len(gp.counts), lib.ws.c, qg.current_stream())
     torch.cuda.synchronize()
-    del bias
+    del bias, qs
     return rc, D
 
 

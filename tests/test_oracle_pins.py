@@ -236,6 +236,17 @@ def test_bias_follows_alpha_and_beta():
     assert np.array_equal(b1, b0 + np.abs(bias)[None, :])
 
 
+def test_output_quantisation_closed_forms():
+    # round half to even, saturation, zero point, NaN -> 0, scale per row
+    x = np.array([[2.5, 3.5, -2.5, -0.5, 1000.0, -1000.0, float("nan"), 0.49999],
+                  [1.0, 1.25, -1.0, 63.5, 64.5, 0.0, 2.0, -3.0]])
+    q = oracle.quantize_s8(x, [1.0, 2.0], 0)
+    assert q[0].tolist() == [2, 4, -2, 0, 127, -128, 0, 0]
+    assert q[1].tolist() == [2, 2, -2, 127, 127, 0, 4, -6]
+    q = oracle.quantize_s8(x[1:], [2.0], -3)
+    assert q[0].tolist() == [-1, -0.0, -5, 124, 126, -3, 1, -9]
+
+
 def test_entries_agree_with_full():
     p = synth.dense(37, 29, 40, seed=21, a_type=BF16, d_type=BF16, alpha=1.5, beta=0.5)
     ref, bound = oracle.gemm(p)
