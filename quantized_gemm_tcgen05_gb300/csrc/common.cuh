@@ -202,17 +202,20 @@ __device__ __forceinline__ float bias_at(const EpiParams& e, int64_t n) {
 }
 
 // Store one output value of row m at element index i: rounded to D's type, or
-// quantised with the row's scale for an int8 D.
+// (Q8) quantised with the row's scale for an int8 D.  Callers choose Q8 once
+// per chunk, so the float store carries no extra per-element test.
+template <bool Q8 = true>
 __device__ __forceinline__ void store_out(const EpiParams& e, int64_t i, float x, int64_t m) {
-    if (e.d_type == DT_S8)
+    if (Q8 && e.d_type == DT_S8)
         static_cast<int8_t*>(e.D)[i] = (int8_t)quant_s8(x, e.qscale[m], e.qzp);
     else
         st_elem(e.D, e.d_type, i, x);
 }
 
 // Four consecutive values of row m (aligned as st4 needs; 4 bytes for int8).
+template <bool Q8 = true>
 __device__ __forceinline__ void store_out4(const EpiParams& e, int64_t i, float4 v, int64_t m) {
-    if (e.d_type == DT_S8) {
+    if (Q8 && e.d_type == DT_S8) {
         const float s = e.qscale[m];
         const uint32_t b = (uint32_t)(quant_s8(v.x, s, e.qzp) & 0xFF) | ((uint32_t)(quant_s8(v.y, s, e.qzp) & 0xFF) << 8) |
                            ((uint32_t)(quant_s8(v.z, s, e.qzp) & 0xFF) << 16) |
@@ -363,7 +366,7 @@ __device__ __forceinline__ void load_c_chunk(const EpiParams& e, const Unit& u, 
 // r = ew*32 + lane, combined with the prefetched C values.  `staging` is this
 // warp's private 32 x W fp32 buffer (swizzled by 16-byte quads) that turns the
 // row-per-thread TMEM layout into row-contiguous global stores.
-template <int W, int ACT>
+template <int W, int ACT, bool Q8>
 __device__ __forceinline__ void store_chunk_t(const EpiParams& e, const Unit& u, int ew, int lane, int col0,
                                             const float (&v)[W], const CChunk<W>& cc, float4* staging) {
     constexpr int Q = W / 4;
@@ -377,7 +380,7 @@ __device__ __forceinline__ void store_chunk_t(const EpiParams& e, const Unit& u,
 #pragma unroll
         for (int j = 0; j < W; ++j) {
             const int64_t m = u.y_row0 + col0 + j;
-            if (m < e.M) store_out(e, boff_d + m * e.ldd + n, epi_value<ACT>(e, v[j], cc.v[j], bn), m);
+            if (m < e.M) store_out<Q8>(e, boff_d + m * e.ldd + n, epi_value<ACT>(e, v[j], cc.v[j], bn), m);
         }
         return;
     }
@@ -408,10 +411,10 @@ __device__ __forceinline__ void store_chunk_t(const EpiParams& e, const Unit& u,
                                      epi_value<ACT>(e, a.z, cc.v[4 * it + 2], bq[2]),
                                      epi_value<ACT>(e, a.w, cc.v[4 * it + 3], bq[3]));
         if (e.vec_ok && n0 + 3 < e.N) {
-            store_out4(e, di, o, m);
+            store_out4<Q8>(e, di, o, m);
         } else {
             const float ov[4] = {o.x, o.y, o.z, o.w};
-            for (int q = 0; q < 4 && n0 + q < e.N; ++q) store_out(e, di + q, ov[q], m);
+            for (int q = 0; q < 4 && n0 + q < e.N; ++q) store_out<Q8>(e, di + q, ov[q], m);
         }
     }
     __syncwarp();
@@ -420,7 +423,10 @@ __device__ __forceinline__ void store_chunk_t(const EpiParams& e, const Unit& u,
 template <int W>
 __device__ __forceinline__ void store_chunk(const EpiParams& e, const Unit& u, int ew, int lane, int col0,
                                             const float (&v)[W], const CChunk<W>& cc, float4* staging) {
-    with_epi_act(e, [&](auto act) { store_chunk_t<W, decltype(act)::value>(e, u, ew, lane, col0, v, cc, staging); });
+    if (e.d_type == DT_S8)
+        with_epi_act(e, [&](auto act) { store_chunk_t<W, decltype(act)::value, true>(e, u, ew, lane, col0, v, cc, staging); });
+    else
+        with_epi_act(e, [&](auto act) { store_chunk_t<W, decltype(act)::value, false>(e, u, ew, lane, col0, v, cc, staging); });
 }
 
 // Partial tile layout in the workspace: for chunk c and quad j, the 128 rows'
