@@ -77,3 +77,36 @@ def test_gemm_create_without_gpu_reports_error():
     import ctypes
     h = ctypes.c_void_p()
     assert qg.lib().gemm_create(ctypes.byref(h)) in (qg.GEMM_ERR_CUDA, qg.GEMM_ERR_UNSUPPORTED)
+
+
+def test_binding_struct_layouts_match_the_header(tmp_path):
+    """The ctypes mirrors of gemm_op_t, gemm_layout_t and gemm_workspace_t have
+    the header's sizes and field offsets (compiled with the host C compiler),
+    and the binding's enum values are the header's."""
+    import ctypes
+    import shutil
+    import subprocess
+
+    if shutil.which("gcc") is None:
+        pytest.skip("no host C compiler")
+    structs = {"gemm_op_t": qg.gemm_op_t, "gemm_layout_t": qg.gemm_layout_t, "gemm_workspace_t": qg.gemm_workspace_t}
+    lines = []
+    for name, cls in structs.items():
+        lines.append(f'printf("{name} size %zu\\n", sizeof({name}));')
+        for field, _ in cls._fields_:
+            lines.append(f'printf("{name}.{field} %zu\\n", offsetof({name}, {field}));')
+    consts = ["GEMM_F32", "GEMM_F16", "GEMM_BF16", "GEMM_S4", "GEMM_S8", "GEMM_EPILOGUE_BIAS", "GEMM_EPILOGUE_RELU",
+              "GEMM_EPILOGUE_GELU", "GEMM_DISPATCH_MEASURE"]
+    lines += [f'printf("{c} %d\\n", (int){c});' for c in consts]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "gemm.h"\nint main(void) {\n' +
+                   "\n".join(lines) + "\nreturn 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = dict(line.rsplit(" ", 1) for line in subprocess.check_output([str(exe)], text=True).splitlines())
+    for name, cls in structs.items():
+        assert int(got[f"{name} size"]) == ctypes.sizeof(cls), name
+        for field, _ in cls._fields_:
+            assert int(got[f"{name}.{field}"]) == getattr(cls, field).offset, f"{name}.{field}"
+    for c in consts:
+        assert int(got[c]) == getattr(qg, c), c
