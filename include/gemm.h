@@ -301,6 +301,20 @@ const char* gemm_last_choice(gemm_handle_t h);
 int gemm_plan_streamk(int64_t m, int64_t n, int64_t k, int32_t block_m, int32_t block_n,
                       int32_t block_k, int32_t total_sm, int64_t out[7]);
 
+/*
+ * Host-only diagnostic: the name (as gemm_last_choice prints it) of the kernel
+ * and schedule the heuristic picks, with no cache entry and no forced
+ * schedule, for a problem of this shape and these types on a device with
+ * sm_count SMs and partials_size bytes of workspace partials.  quant_a_group /
+ * quant_b_group > 0 mean U / V scales; num_experts > 0 describes a grouped
+ * problem with m rows in total.  Needs no GPU.  Writes a NUL-terminated name
+ * of at most cap bytes to out; returns GEMM_ERR_INVALID_ARG for bad arguments
+ * or a too small buffer.
+ */
+int gemm_heuristic_choice(int64_t m, int64_t n, int64_t k, int32_t a_type, int32_t b_type, int32_t d_type,
+                          int32_t quant_a_group, int32_t quant_b_group, int32_t num_experts, int32_t sm_count,
+                          size_t partials_size, char* out, size_t cap);
+
 /* gemm_grouped_block: the grouped tile map (same page, section gemm_grouped)
  * for padded M-block `block` of experts with `sizes[0..E-1]` rows:
  * out[0] = expert, out[1] = first row, out[2] = rows (0 past the last block).

@@ -40,7 +40,7 @@ SYMBOLS = (
     "gemm_create", "gemm_destroy", "gemm_run", "gemm_run_grouped", "gemm_export", "gemm_import",
     "gemm_get_tuning_seq", "gemm_cache_size", "gemm_status_string", "gemm_device_status",
     "gemm_selftest_wait_timeout", "gemm_last_choice", "gemm_plan_streamk", "gemm_grouped_block",
-    "gemm_run_noalloc",
+    "gemm_run_noalloc", "gemm_heuristic_choice",
 )
 
 
@@ -105,6 +105,8 @@ def lib():
         "gemm_last_choice": (ctypes.c_char_p, [P]),
         "gemm_plan_streamk": (ctypes.c_int, [I64, I64, I64, I32, I32, I32, I32, ctypes.POINTER(I64)]),
         "gemm_grouped_block": (ctypes.c_int, [ctypes.POINTER(I32), I32, I32, I64, ctypes.POINTER(I64)]),
+        "gemm_heuristic_choice": (ctypes.c_int, [I64, I64, I64, I32, I32, I32, I32, I32, I32, I32, ctypes.c_size_t,
+                                                 ctypes.c_char_p, ctypes.c_size_t]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -212,6 +214,17 @@ def gemm_plan_streamk(m, n, k, block_m, block_n, block_k, total_sm):
     keys = ("iters_per_tile", "total_tiles", "streamk_tiles", "blocking_tiles", "full_tiles", "partial_tiles",
             "sm_partition_factor")
     return dict(zip(keys, list(out)))
+
+
+def gemm_heuristic_choice(m, n, k, a_type, b_type, d_type, quant_a_group=0, quant_b_group=0, num_experts=0,
+                          sm_count=152, partials_size=GEMM_PARTIALS_SIZE):
+    """The kernel / schedule name the heuristic picks for this problem (host only)."""
+    buf = ctypes.create_string_buffer(96)
+    rc = lib().gemm_heuristic_choice(m, n, k, a_type, b_type, d_type, quant_a_group, quant_b_group, num_experts,
+                                     sm_count, partials_size, buf, len(buf))
+    if rc:
+        raise GemmError(rc, "gemm_heuristic_choice")
+    return buf.value.decode()
 
 
 def gemm_grouped_block(sizes, block_m, block):

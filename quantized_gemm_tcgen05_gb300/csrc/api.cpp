@@ -964,6 +964,57 @@ int gemm_plan_streamk(int64_t m, int64_t n, int64_t k, int32_t block_m, int32_t 
     return GEMM_OK;
 }
 
+int gemm_heuristic_choice(int64_t m, int64_t n, int64_t k, int32_t a_type, int32_t b_type, int32_t d_type,
+                          int32_t quant_a_group, int32_t quant_b_group, int32_t num_experts, int32_t sm_count,
+                          size_t partials_size, char* out, size_t cap) {
+    if (!out || cap == 0 || m < 1 || n < 1 || k < 1 || sm_count < 1 || num_experts < 0) return GEMM_ERR_INVALID_ARG;
+    if (!is16(a_type) || !(b_type == a_type || b_type == GEMM_S4)) return GEMM_ERR_INVALID_ARG;
+    if (!is_float_out(d_type) && d_type != GEMM_S8) return GEMM_ERR_INVALID_ARG;
+    Problem p;
+    memset(&p, 0, sizeof p);
+    p.M = m;
+    p.N = n;
+    p.K = k;
+    p.a_type = a_type;
+    p.b_type = b_type;
+    p.d_type = d_type;
+    p.batches = 1;
+    // the heuristic only asks whether scales are present: a marker stands in
+    static const int32_t marker = 0;
+    if (quant_a_group > 0) {
+        p.U = &marker;
+        p.ga = quant_a_group;
+    }
+    if (quant_b_group > 0) {
+        p.V = &marker;
+        p.gb = quant_b_group;
+    }
+    p.family = (p.U || p.V || b_type == GEMM_S4) ? FAM_DQ : FAM_DENSE;
+    if (num_experts > 0) {
+        if (p.family != FAM_DENSE) return GEMM_ERR_INVALID_ARG;
+        p.family = FAM_GROUPED;
+        p.num_experts = num_experts;
+    }
+    Choice c = heuristic(p, sm_count, partials_size);
+    // the automatic fallbacks of dispatch_and_run when the workspace is too small
+    auto fits = [&](const Choice& x) {
+        if (x.gemv) return true;
+        const SchedParams sp = make_sched(p, x, sm_count);
+        return partials_bytes_needed(sp, x.bn, x.pair) <= partials_size;
+    };
+    if (p.family == FAM_GROUPED) c.sched = SCHED_DP;
+    if (!fits(c) && c.sched != SCHED_DP && !c.swap && c.bn > 128) {
+        Choice narrower = c;
+        narrower.bn = 128;
+        if (fits(narrower)) c = narrower;
+    }
+    if (!fits(c)) c.sched = SCHED_DP;
+    const std::string name = choice_name(p, c);
+    if (name.size() + 1 > cap) return GEMM_ERR_INVALID_ARG;
+    memcpy(out, name.c_str(), name.size() + 1);
+    return GEMM_OK;
+}
+
 int gemm_grouped_block(const int32_t* sizes, int32_t num_experts, int32_t block_m, int64_t block,
                        int64_t out[3]) {
     if (!sizes || !out || num_experts < 1 || block_m <= 0 || block < 0) return GEMM_ERR_INVALID_ARG;

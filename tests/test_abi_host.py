@@ -110,3 +110,28 @@ def test_binding_struct_layouts_match_the_header(tmp_path):
             assert int(got[f"{name}.{field}"]) == getattr(cls, field).offset, f"{name}.{field}"
     for c in consts:
         assert int(got[c]) == getattr(qg, c), c
+
+
+@pytest.mark.parametrize("args,want", [
+    # the benchmark workloads on a 152-SM GB300 with the 32 MB partials buffer
+    ((256, 256, 256, qg.GEMM_F16, qg.GEMM_F16, qg.GEMM_F32), "umma_bn128/splitk8"),
+    ((4096, 4096, 4096, qg.GEMM_BF16, qg.GEMM_BF16, qg.GEMM_BF16), "umma2_bn224/dp"),
+    ((1, 4096, 14336, qg.GEMM_BF16, qg.GEMM_BF16, qg.GEMM_BF16), "gemv"),
+    ((16, 4096, 14336, qg.GEMM_BF16, qg.GEMM_BF16, qg.GEMM_BF16), "umma_bn16_swap/splitk4"),
+    ((64, 4096, 14336, qg.GEMM_BF16, qg.GEMM_BF16, qg.GEMM_BF16), "umma_bn64_swap/splitk4"),
+    ((128, 11008, 4096, qg.GEMM_BF16, qg.GEMM_S4, qg.GEMM_BF16, 0, 128), "umma_dq_bn128/streamk"),
+    ((1, 11008, 4096, qg.GEMM_BF16, qg.GEMM_S4, qg.GEMM_BF16, 0, 128), "gemv"),
+    ((4096, 14336, 4096, qg.GEMM_BF16, qg.GEMM_BF16, qg.GEMM_BF16, 0, 0, 8), "umma2_grouped_bn256/dp"),
+])
+def test_heuristic_choices_of_the_workloads(args, want):
+    assert qg.gemm_heuristic_choice(*args) == want
+
+
+def test_heuristic_choice_rejects_bad_arguments():
+    with pytest.raises(qg.GemmError):
+        qg.gemm_heuristic_choice(0, 16, 16, qg.GEMM_BF16, qg.GEMM_BF16, qg.GEMM_BF16)
+    with pytest.raises(qg.GemmError):
+        qg.gemm_heuristic_choice(16, 16, 16, qg.GEMM_BF16, qg.GEMM_F16, qg.GEMM_BF16)
+    # a workspace too small for a split falls back to the unsplit schedule
+    assert qg.gemm_heuristic_choice(16, 4096, 14336, qg.GEMM_BF16, qg.GEMM_BF16, qg.GEMM_BF16,
+                                    partials_size=0) == "umma_bn16_swap/dp"
