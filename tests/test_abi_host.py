@@ -135,3 +135,19 @@ def test_heuristic_choice_rejects_bad_arguments():
     # a workspace too small for a split falls back to the unsplit schedule
     assert qg.gemm_heuristic_choice(16, 4096, 14336, qg.GEMM_BF16, qg.GEMM_BF16, qg.GEMM_BF16,
                                     partials_size=0) == "umma_bn16_swap/dp"
+
+
+def test_small_m_kernel_limits(monkeypatch):
+    # M <= 2 by default; U scales and grouped problems never take it; the
+    # environment limit moves or removes it
+    bf = qg.GEMM_BF16
+    assert qg.gemm_heuristic_choice(2, 4096, 4096, bf, bf, bf) == "gemv"
+    assert qg.gemm_heuristic_choice(3, 4096, 4096, bf, bf, bf) != "gemv"
+    assert qg.gemm_heuristic_choice(1, 4096, 4096, bf, bf, bf, quant_a_group=128) != "gemv"
+    assert qg.gemm_heuristic_choice(1, 4096, 4096, bf, bf, bf, num_experts=4) != "gemv"
+    assert qg.gemm_heuristic_choice(1, 4096, 4096, bf, qg.GEMM_S4, qg.GEMM_S8, quant_b_group=64) == "gemv"
+    monkeypatch.setenv("GEMM_GEMV_MAX_M", "0")
+    assert qg.gemm_heuristic_choice(1, 4096, 4096, bf, bf, bf) != "gemv"
+    monkeypatch.setenv("GEMM_GEMV_MAX_M", "8")
+    assert qg.gemm_heuristic_choice(8, 4096, 4096, bf, bf, bf) == "gemv"
+    assert qg.gemm_heuristic_choice(9, 4096, 4096, bf, bf, bf) != "gemv"
