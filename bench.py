@@ -74,7 +74,21 @@ WORKLOADS = {
 }
 
 
+def register_shape(shape):
+    """Add a dense bf16 workload of the given "M,N,K" with C2's recipe; returns its name."""
+    M, N, K = (int(x) for x in shape.split(","))
+    if min(M, N, K) < 1:
+        raise ValueError(f"bad shape {shape!r}")
+    cfg = f"dense{M}x{N}x{K}"
+    WORKLOADS[cfg] = dict(desc=f"dense bf16 GEMM M={M} N={N} K={K}, A row-major, B col-major, N(0,1)/sqrt(K), "
+                               f"C bf16 N(0,1), alpha 1.5 beta 0.5, bf16 D", kind="dense", shape=(M, N, K))
+    return cfg
+
+
 def make_problem(cfg):
+    if "shape" in WORKLOADS.get(cfg, {}):
+        M, N, K = WORKLOADS[cfg]["shape"]
+        return synth.config2(M=M, N=N, K=K)
     if cfg == "c1":
         return synth.config1()
     if cfg == "c2":
@@ -541,7 +555,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--launch", choices=["graph", "eager"], default="graph")
+    ap.add_argument("--shape", help="M,N,K: a dense bf16 problem of this shape with C2's recipe, instead of --config")
     args = ap.parse_args()
+    if args.shape:
+        args.config = register_shape(args.shape)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank = int(os.environ.get("RANK", "0"))

@@ -63,3 +63,16 @@ def test_single_process_needs_no_group():
 
     assert bench.max_over_ranks(3.5, None) == 3.5
     assert bench.job_throughput(2.0, 4, 1, 8.0) == pytest.approx(2.0 * 4 / 8e-3)
+
+
+def test_custom_dense_shape_uses_the_c2_recipe():
+    import bench
+    import synth
+
+    cfg = bench.register_shape("96,40,24")
+    p = bench.make_problem(cfg)
+    ref = synth.config2(M=96, N=40, K=24)
+    assert (p.M, p.N, p.K) == (96, 40, 24)
+    assert (p.A == ref.A).all() and (p.B == ref.B).all() and (p.C == ref.C).all()
+    assert (p.alpha, p.beta) == (1.5, 0.5)
+    assert "M=96 N=40 K=24" in bench.WORKLOADS[cfg]["desc"]
