@@ -237,11 +237,11 @@ class ClockSampler:
 class Runner:
     """Device buffers plus pre-built ctypes arguments for repeated gemm_run calls."""
 
-    def __init__(self, p, sets, qg, torch):
+    def __init__(self, p, sets, qg, torch, splitk=0, streamk=0):
         self.p, self.qg, self.torch = p, qg, torch
         self.h = qg.gemm_create()
         self.ws = qg.Workspace()
-        self.op = qg.gemm_op_t(0, 0, 0, p.gb if getattr(p, "V", None) is not None else 0, 0, 0)
+        self.op = qg.gemm_op_t(0, 0, 0, p.gb if getattr(p, "V", None) is not None else 0, splitk, streamk)
         self.stream = qg.current_stream()
         self.grouped = hasattr(p, "counts")
         self.args = []
@@ -294,6 +294,141 @@ class Runner:
             raise RuntimeError(f"gemm_run failed: {qg.gemm_status_string(rc)}")
 
 
+def input_sets(cfg, one_set):
+    """Rotating copies of the inputs so that consecutive steps do not find
+    their operands in the 129 MB L2: at least 3 x L2 in total (at most 8)."""
+    if cfg == "c2":
+        return 3
+    return max(1, min(8, int(np.ceil(3 * 129e6 / max(one_set, 1)))))
+
+
+def time_steps(R, sets, steps, launch, torch, qg, barrier, soak_s=0.0):
+    """Time exactly `steps` calls of R.run on the current stream.
+
+    graph: the calls are captured once into a CUDA graph (as an engine
+    replaying its layers would), replayed untimed (for at least soak_s seconds,
+    so clock samples see the load), then timed as one replay.  eager: one
+    gemm_run per step with CUDA events around every launch.  Returns
+    (total_ms, per-launch ms or None, t0, t1) with t0/t1 the wall-clock window
+    of the untimed soak plus the timed region."""
+    stream = torch.cuda.current_stream()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if launch == "graph":
+        cap = torch.cuda.Stream()
+        graph = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(steps):
+                R.run(i % sets, qg.current_stream())
+        torch.cuda.synchronize()
+        t0 = time.time()
+        graph.replay()
+        torch.cuda.synchronize()
+        while time.time() - t0 < soak_s:
+            graph.replay()
+            torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        graph.replay()
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        t1 = time.time()
+        del graph
+        return start.elapsed_time(end), None, t0, t1
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for i in range(steps):
+        evs[i][0].record(stream)
+        R.run(i % sets)
+        evs[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t1 = time.time()
+    return start.elapsed_time(end), [a.elapsed_time(b) for a, b in evs], t0, t1
+
+
+def roofline_of(cfg, p, avg_launch_s, traffic, peaks, peak_src):
+    """The roofline object for one workload: achieved algorithmic bytes or
+    flops per launch over the launch's duration, against the measured peak."""
+    flops, abytes = flops_of(p), algorithmic_bytes(p)
+    _, _, bound = metric_of(cfg)
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    if bound == "hbm":
+        achieved, peak, r_unit = abytes / avg_launch_s / 1e9, hbm_peak, "GB/s"
+    else:
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) * tensor_peak_ratio(p)
+        achieved, r_unit = flops / avg_launch_s / 1e12, "TFLOP/s"
+    r = {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": r_unit,
+         "frac": round(achieved / peak, 4), "traffic": traffic,
+         "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
+                        + ("" if tensor_peak_ratio(p) == 1 else f" x {tensor_peak_ratio(p):g} (nominal dense ratio of "
+                                                                  f"this input type to bf16)"),
+         "algorithmic_per_launch": abytes if bound == "hbm" else flops,
+         "avg_launch_us": round(avg_launch_s * 1e6, 3)}
+    if bound == "tensor":
+        r["hbm_gbs"] = round(abytes / avg_launch_s / 1e9, 1)
+        r["hbm_frac"] = round(abytes / avg_launch_s / 1e9 / hbm_peak, 4)
+        r["min_roofline_us"] = round(max(flops / (peak * 1e12), abytes / (hbm_peak * 1e9)) * 1e6, 3)
+        r["min_roofline_frac"] = round(r["min_roofline_us"] / (avg_launch_s * 1e6), 4)
+    return r
+
+
+def tensor_peak_ratio(p):
+    """Nominal dense tensor rate of the problem's input type relative to bf16
+    (fp8: 4.5 / 2.25 PFLOP/s)."""
+    return 2.0 if getattr(p, "a_type", None) in (synth.E4M3, synth.E5M2) else 1.0
+
+
+SCHEDULES = {"auto": (0, 0), "unsplit": (1, 0), "splitk8": (8, 0), "streamk": (0, 1)}
+
+# Workloads measured beside the headline, each in the same process: the
+# decode shapes under every schedule the decode workload names, plus the
+# automatic choice.
+SUB_CONFIGS = ([("c1", "auto")] +
+               [(f"c3m{m}", s) for m in (1, 16, 64) for s in ("auto", "unsplit", "splitk8", "streamk")] +
+               [("c4", "auto"), ("c5", "auto")])
+
+
+def measure_config(cfg, sched, steps, warmup, launch, sampler, peaks, peak_src, qg, torch, p=None):
+    """One workload under one schedule, timed like the headline; returns its
+    entry of the "configs" object."""
+    p = make_problem(cfg) if p is None else p
+    metric, unit, bound = metric_of(cfg)
+    abytes, flops = algorithmic_bytes(p), flops_of(p)
+    sets = input_sets(cfg, abytes)
+    splitk, streamk = SCHEDULES[sched]
+    R = Runner(p, sets, qg, torch, splitk=splitk, streamk=streamk)
+    try:
+        for i in range(warmup):
+            R.run(i % sets)
+        torch.cuda.synchronize()
+        if qg.gemm_device_status(R.h, R.stream):
+            raise RuntimeError(f"{cfg}/{sched}: device status reported a timeout during warm-up")
+        choice = qg.gemm_last_choice(R.h)
+        total_ms, launch_ms, t0, t1 = time_steps(R, sets, steps, launch, torch, qg, lambda: None, soak_s=0.2)
+        if qg.gemm_device_status(R.h, R.stream):
+            raise RuntimeError(f"{cfg}/{sched}: device status reported a timeout")
+    finally:
+        qg.gemm_destroy(R.h)
+    avg_launch_s = (statistics.mean(launch_ms) if launch_ms else total_ms / steps) / 1e3
+    unit_per_step = abytes / 1e9 if unit == "GB/s" else flops / 1e12
+    traffic = profile_traffic(cfg, choice)
+    entry = {"workload": WORKLOADS[cfg]["desc"], "schedule": sched, "kernel": choice, "metric": metric,
+             "value": round(job_throughput(unit_per_step, steps, 1, total_ms), 3), "unit": unit,
+             "steps": steps, "ms_per_step": round(total_ms / steps, 5), "gpu_launches": steps,
+             "roofline": roofline_of(cfg, p, avg_launch_s, traffic, peaks, peak_src),
+             "clocks": sampler.summary(t0, t1)}
+    del R
+    torch.cuda.empty_cache()
+    return entry
+
+
 def run_ours(args, rank, world, cfg):
     import torch
 
@@ -311,10 +446,8 @@ def run_ours(args, rank, world, cfg):
     metric, unit, bound = metric_of(cfg)
     unit_per_step = abytes / 1e9 if unit == "GB/s" else flops / 1e12
     one_set = abytes
-    sets = max(1, min(8, int(np.ceil(3 * 129e6 / max(one_set, 1)))))
-    sets = 3 if cfg == "c2" else sets
+    sets = input_sets(cfg, one_set)
     R = Runner(p, sets, qg, torch)
-    stream = torch.cuda.current_stream()
 
     def barrier():
         if dist is not None:
@@ -330,50 +463,9 @@ def run_ours(args, rank, world, cfg):
         raise RuntimeError("device status reported a timeout during warm-up")
     choice = qg.gemm_last_choice(R.h)
 
-    # timed region: K steps.  Eager: one gemm_run per step with CUDA events
-    # around every launch on the launching stream.  Graph: the K gemm_run
-    # calls captured once into a CUDA graph (as an engine replaying its layers
-    # would), replayed once untimed, then timed as one replay.
-    launch_ms = None
-    if args.launch == "graph":
-        cap = torch.cuda.Stream()
-        graph = torch.cuda.CUDAGraph()
-        torch.cuda.synchronize()
-        with torch.cuda.graph(graph, stream=cap):
-            for i in range(args.steps):
-                R.run(i % sets, qg.current_stream())
-        graph.replay()
-        torch.cuda.synchronize()
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier()
-        torch.cuda.synchronize()
-        t0 = time.time()
-        start.record(stream)
-        graph.replay()
-        end.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        t1 = time.time()
-        total_ms = start.elapsed_time(end)
-    else:
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier()
-        torch.cuda.synchronize()
-        t0 = time.time()
-        start.record(stream)
-        for i in range(args.steps):
-            evs[i][0].record(stream)
-            R.run(i % sets)
-            evs[i][1].record(stream)
-        end.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        t1 = time.time()
-        total_ms = start.elapsed_time(end)
-        launch_ms = [a.elapsed_time(b) for a, b in evs]
-    sampler.stop()
+    # timed region: exactly K steps (see time_steps)
+    total_ms, launch_ms, t0, t1 = time_steps(R, sets, args.steps, args.launch, torch, qg, barrier, soak_s=0.3)
+    clocks = sampler.summary(t0, t1)
     total_ms = max_over_ranks(total_ms, dist)
     ms_per_step = total_ms / args.steps
     value = job_throughput(unit_per_step, args.steps, world, total_ms)
@@ -391,42 +483,43 @@ def run_ours(args, rank, world, cfg):
     # graph replay divided by its launches (back-to-back kernels, so this also
     # charges the inter-kernel gaps to the kernel: a conservative figure)
     avg_launch_s = (statistics.mean(launch_ms) if launch_ms else ms_per_step) / 1e3
-    if bound == "hbm":
-        achieved = abytes / avg_launch_s / 1e9
-        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        r_unit = "GB/s"
-    else:
-        achieved = flops / avg_launch_s / 1e12
-        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-        r_unit = "TFLOP/s"
     traffic = profile_traffic(cfg, choice)
-    clocks = sampler.summary(t0, t1)
     line = {
         "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if p.a_type == synth.BF16 else "f16",
+        "scaling": "weak", "vs_baseline": None, "dtype": synth.DTYPE_NAMES.get(p.a_type, "bf16"),
         "data": "synthetic (seeded, shapes and distributions of the workload)",
         "config": {"workload": WORKLOADS[cfg]["desc"], "kernel": choice, "parallelism": f"replicas x{world}",
                    "launch": "CUDA graph of the K gemm_run calls" if args.launch == "graph" else "eager gemm_run per step",
                    "l2": f"{sets} rotating input sets ({sets * one_set / 1e6:.0f} MB) so operands are not L2-resident"},
-        "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": r_unit,
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})",
-                     "algorithmic_per_launch": abytes if bound == "hbm" else flops,
-                     "avg_launch_us": round(avg_launch_s * 1e6, 3)},
+        "roofline": roofline_of(cfg, p, avg_launch_s, traffic, peaks, peak_src),
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": args.steps,
     }
-    if bound == "tensor":
-        hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        line["roofline"]["hbm_gbs"] = round(abytes / avg_launch_s / 1e9, 1)
-        line["roofline"]["min_roofline_us"] = round(max(flops / (peak * 1e12), abytes / (hbm_peak * 1e9)) * 1e6, 3)
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(p, cfg, unit)
+    R.qg.gemm_destroy(R.h)
+    del R
+    torch.cuda.empty_cache()
+    # the other workloads, one process, after the headline (one GPU only)
+    if world == 1 and not args.no_configs:
+        sub_steps = max(3, min(20, args.steps))
+        configs = {}
+        made = {}
+        for c, s in SUB_CONFIGS:
+            if c == cfg and s == "auto":
+                continue
+            if c not in made:
+                made.clear()
+                made[c] = make_problem(c)
+            key = c if s == "auto" else f"{c}/{s}"
+            configs[key] = measure_config(c, s, sub_steps, 3, args.launch, sampler, peaks, peak_src, qg, torch,
+                                          p=made[c])
+        line["configs"] = configs
+    sampler.stop()
     if dist is not None:
         dist.destroy_process_group()
-    R.qg.gemm_destroy(R.h)
     return line
 
 
@@ -554,6 +647,7 @@ def main():
     ap.add_argument("--config", choices=sorted(WORKLOADS), default="c2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="time only the --config workload")
     ap.add_argument("--launch", choices=["graph", "eager"], default="graph")
     ap.add_argument("--shape", help="M,N,K: a dense bf16 problem of this shape with C2's recipe, instead of --config")
     args = ap.parse_args()

@@ -87,7 +87,9 @@ typedef struct {
 enum {
     GEMM_DISPATCH_DEFAULT = 0, /* cache hit, else the heuristic                   */
     GEMM_DISPATCH_MEASURE = 1, /* on a miss, time the candidates on the stream
-                                  (synchronises it) and store the winner        */
+                                  (synchronises it) and store the winner; on a
+                                  stream that is being captured nothing is
+                                  timed: the cache, else the heuristic         */
     GEMM_DISPATCH_REUSE = 2    /* cache only (no measuring), else the heuristic   */
 };
 
@@ -194,9 +196,10 @@ int gemm_run(gemm_handle_t h, const gemm_op_t* op, float alpha,
 
 /*
  * gemm_run without a workspace argument, for callers that cannot allocate
- * device memory (for example code running under a stream capture that forbids
- * allocation, or inside a host whose allocator hands out no scratch).  The
- * pages have no counterpart to this entry point.
+ * device memory: for example a plug-in inside a host framework whose caching
+ * allocator owns all device memory and hands out no scratch, or code on a
+ * latency-critical path where an allocation would synchronise the device.
+ * The pages have no counterpart to this entry point.
  *   - Scratch for split-K / stream-K comes from a fixed array in the library's
  *     own device memory: 64 KB of tile counters and 8 MB of fp32 partials
  *     (GEMM_NOALLOC_BARRIERS_SIZE / GEMM_NOALLOC_PARTIALS_SIZE).  Every GPU

@@ -604,6 +604,26 @@ bool forced_kernel(const Problem& p, Choice* out) {
     return true;
 }
 
+// The last step of an automatic choice, shared by gemm_run and the host-only
+// gemm_heuristic_choice: grouped problems run data-parallel; a split whose
+// partials do not fit the workspace first tries half-width tiles, then (when
+// the schedule was not forced) runs unsplit.  Returns false when a forced
+// schedule does not fit.
+template <typename Fits>
+bool settle_schedule(const Problem& p, Choice* c, bool forced, const Fits& fits) {
+    if (p.family == FAM_GROUPED) c->sched = SCHED_DP;
+    if (!fits(*c) && c->sched != SCHED_DP && !c->swap && c->bn > 128) {
+        Choice narrower = *c;  // half-width tiles halve the partial-tile footprint
+        narrower.bn = 128;
+        if (fits(narrower)) *c = narrower;
+    }
+    if (!fits(*c)) {
+        if (forced) return false;
+        c->sched = SCHED_DP;  // automatic choices fall back to no split
+    }
+    return true;
+}
+
 int dispatch_and_run(gemm_handle* h, const gemm_op_t* op, Problem& p, const gemm_workspace_t* ws, cudaStream_t st) {
     if (p.M == 0 || p.N == 0) {
         h->last_choice = "empty";
@@ -644,7 +664,26 @@ int dispatch_and_run(gemm_handle* h, const gemm_op_t* op, Problem& p, const gemm
             have = workspace_fits(h, p, c, ws);
         }
     }
-    if (!have && !forced && op->dispatch == GEMM_DISPATCH_MEASURE) {
+    // measuring synchronises the stream, which a stream capture forbids: a
+    // measuring call on a capturing stream uses the cache or the heuristic
+    bool measure_ok = op->dispatch == GEMM_DISPATCH_MEASURE;
+    if (measure_ok) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+            cudaGetLastError();
+            measure_ok = false;
+        } else if (cs != cudaStreamCaptureStatusNone) {
+            measure_ok = false;
+        }
+    }
+    if (!have && !forced && op->dispatch == GEMM_DISPATCH_MEASURE && !measure_ok) {
+        auto it = h->cache.find(key);
+        if (it != h->cache.end()) {
+            c = it->second;
+            have = workspace_fits(h, p, c, ws);
+        }
+    }
+    if (!have && !forced && measure_ok) {
         auto it = h->cache.find(key);
         if (it != h->cache.end() && workspace_fits(h, p, it->second, ws)) {
             c = it->second;
@@ -675,16 +714,8 @@ int dispatch_and_run(gemm_handle* h, const gemm_op_t* op, Problem& p, const gemm
         } else if (op->splitk == 1 || op->streamk == -1) {
             if (c.sched != SCHED_DP && (op->splitk == 1 || c.sched == SCHED_STREAMK)) c.sched = SCHED_DP;
         }
-        if (p.family == FAM_GROUPED) c.sched = SCHED_DP;
-        if (!workspace_fits(h, p, c, ws) && c.sched != SCHED_DP && !c.swap && c.bn > 128) {
-            Choice narrower = c;  // half-width tiles halve the partial-tile footprint
-            narrower.bn = 128;
-            if (workspace_fits(h, p, narrower, ws)) c = narrower;
-        }
-        if (!workspace_fits(h, p, c, ws)) {
-            if (forced) return GEMM_ERR_WORKSPACE;
-            c.sched = SCHED_DP;  // automatic choices fall back to no split
-        }
+        if (!settle_schedule(p, &c, forced, [&](const Choice& x) { return workspace_fits(h, p, x, ws); }))
+            return GEMM_ERR_WORKSPACE;
     }
     h->last_choice = choice_name(p, c);
     if (h->log)
@@ -996,19 +1027,15 @@ int gemm_heuristic_choice(int64_t m, int64_t n, int64_t k, int32_t a_type, int32
         p.num_experts = num_experts;
     }
     Choice c = heuristic(p, sm_count, partials_size);
-    // the automatic fallbacks of dispatch_and_run when the workspace is too small
-    auto fits = [&](const Choice& x) {
+    // the automatic fallbacks of dispatch_and_run, against a workspace of
+    // partials_size bytes of partials and a barrier buffer of the usual size
+    // (on this path every program count is sm_count)
+    settle_schedule(p, &c, false, [&](const Choice& x) {
         if (x.gemv) return true;
         const SchedParams sp = make_sched(p, x, sm_count);
-        return partials_bytes_needed(sp, x.bn, x.pair) <= partials_size;
-    };
-    if (p.family == FAM_GROUPED) c.sched = SCHED_DP;
-    if (!fits(c) && c.sched != SCHED_DP && !c.swap && c.bn > 128) {
-        Choice narrower = c;
-        narrower.bn = 128;
-        if (fits(narrower)) c = narrower;
-    }
-    if (!fits(c)) c.sched = SCHED_DP;
+        return partials_bytes_needed(sp, x.bn, x.pair) <= partials_size &&
+               counters_bytes_needed(sp, x.pair) <= GEMM_BARRIERS_SIZE;
+    });
     const std::string name = choice_name(p, c);
     if (name.size() + 1 > cap) return GEMM_ERR_INVALID_ARG;
     memcpy(out, name.c_str(), name.size() + 1);

@@ -1,9 +1,9 @@
 // gemm_run_noalloc: gemm_run for callers that cannot allocate device memory.
 //
-// Some callers cannot call cudaMalloc at all -- code that runs while a CUDA
-// graph is being captured in a mode that forbids allocation, allocators that
-// own every byte of the device and hand out no scratch, or plug-in hosts whose
-// memory policy forbids it.  gemm_run needs no allocation either, but its
+// Some callers cannot call cudaMalloc at all: a plug-in inside a host
+// framework whose caching allocator owns every byte of the device and hands
+// out no scratch, or code on a latency-critical path where an allocation
+// would synchronise the device.  gemm_run needs no allocation either, but its
 // split-K / stream-K schedules need a caller-provided workspace.  This entry
 // point supplies that workspace from a fixed array in the library's own
 // device memory instead, so the caller passes only inputs and outputs.
@@ -16,8 +16,10 @@
 
 namespace {
 
-constexpr size_t kNoallocBarriers = 64u << 10;  // 16384 per-tile arrival counters
-constexpr size_t kNoallocPartials = 8u << 20;   // 8 MB of fp32 partial tiles
+constexpr size_t kNoallocBarriers = GEMM_NOALLOC_BARRIERS_SIZE;  // 16384 per-tile arrival counters
+constexpr size_t kNoallocPartials = GEMM_NOALLOC_PARTIALS_SIZE;  // 8 MB of fp32 partial tiles
+static_assert(kNoallocBarriers == (64u << 10) && kNoallocPartials == (8u << 20),
+              "the documented limits of gemm_run_noalloc");
 
 // Every GPU that loads the library holds this array until the process exits.
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBarriers + kNoallocPartials];

@@ -26,8 +26,8 @@ from __future__ import annotations
 import dataclasses
 import numpy as np
 
-F32, F16, BF16, S4, S8 = 0, 1, 2, 3, 4
-DTYPE_NAMES = {F32: "f32", F16: "f16", BF16: "bf16", S4: "s4"}
+F32, F16, BF16, S4, S8, E4M3, E5M2 = 0, 1, 2, 3, 4, 5, 6
+DTYPE_NAMES = {F32: "f32", F16: "f16", BF16: "bf16", S4: "s4", S8: "s8", E4M3: "e4m3", E5M2: "e5m2"}
 
 
 def _round_bits(x: np.ndarray, dtype: int) -> np.ndarray:

@@ -96,7 +96,8 @@ def test_binding_struct_layouts_match_the_header(tmp_path):
         for field, _ in cls._fields_:
             lines.append(f'printf("{name}.{field} %zu\\n", offsetof({name}, {field}));')
     consts = ["GEMM_F32", "GEMM_F16", "GEMM_BF16", "GEMM_S4", "GEMM_S8", "GEMM_EPILOGUE_BIAS", "GEMM_EPILOGUE_RELU",
-              "GEMM_EPILOGUE_GELU", "GEMM_DISPATCH_MEASURE"]
+              "GEMM_EPILOGUE_GELU", "GEMM_DISPATCH_MEASURE", "GEMM_BARRIERS_SIZE", "GEMM_PARTIALS_SIZE",
+              "GEMM_NOALLOC_BARRIERS_SIZE", "GEMM_NOALLOC_PARTIALS_SIZE"]
     lines += [f'printf("{c} %d\\n", (int){c});' for c in consts]
     src = tmp_path / "layout.c"
     src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "gemm.h"\nint main(void) {\n' +
