@@ -11,6 +11,9 @@ Sources, by page and section:
     "InternLM Lmdeploy Gemm Interface", Description / Signature / Usage Examples.
   * Scale operands advance at K-group boundaries: "InternLM Lmdeploy Gemm
     MainloopSm80V2", Description.
+  * FP8 (E4M3 / E5M2) operands: DeepGEMM kernel-set blog, sections 1.2 and
+    6.3 (quantised INT8/FP8 inputs; the FP8 path as the extension that pays
+    off most on new hardware).
   * split-K, stream-K plan, grouped (MoE) tile map and batched flattening:
     TileLang tutorial "gemm_variants.py", sections gemm_splitk, gemm_streamk,
     streamk_plan, gemm_grouped, gemm_batched.
@@ -29,7 +32,8 @@ import threading
 
 import numpy as np
 
-F32, F16, BF16, S4 = 0, 1, 2, 3
+F32, F16, BF16, S4, S8, E4M3, E5M2 = 0, 1, 2, 3, 4, 5, 6
+FP8 = (E4M3, E5M2)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemm_oracle.c")
@@ -91,7 +95,7 @@ def num_threads() -> int:
 # ---- scalar formats --------------------------------------------------------
 
 def decode(dtype: int, bits) -> np.ndarray:
-    """Exact value of stored fp16/bf16/fp32 bit patterns, as float64."""
+    """Exact value of stored fp16/bf16/fp32 or E4M3/E5M2 bit patterns, as float64."""
     L = lib()
     flat = np.asarray(bits).reshape(-1)
     out = np.fromiter((L.oracle_decode(dtype, int(b)) for b in flat), dtype=np.float64, count=flat.size)
@@ -140,12 +144,15 @@ def _desc(p, keep):
     """Build the C problem struct from a synth.Problem-like object."""
     g = _Gemm()
     g.M, g.N, g.K = p.M, p.N, p.K
-    A = _arr(p.A, np.uint16)
+    A = _arr(p.A, np.uint8 if p.a_type in FP8 else np.uint16)
     keep.append(A)
     g.a_type, g.A, g.lda = p.a_type, A.ctypes.data, p.K
     if p.b_type == S4:
         B = _arr(p.B, np.uint8)
         g.ldb = p.K // 2
+    elif p.b_type in FP8:
+        B = _arr(p.B, np.uint8)
+        g.ldb = p.K
     else:
         B = _arr(p.B, np.uint16)
         g.ldb = p.K

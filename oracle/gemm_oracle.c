@@ -14,6 +14,9 @@
  *    DeepGEMM kernel-set blog, section 1.1.
  *  - U/V are group-wise scales that advance at K-group boundaries:
  *    "InternLM Lmdeploy Gemm MainloopSm80V2", section Description (GroupIter).
+ *  - FP8 (E4M3 / E5M2) operands, among the quantised inputs the DeepGEMM
+ *    kernel-set blog targets (sections 1.2 and 6.3): decoded exactly like the
+ *    16-bit ones; every product of two of them is exact in double.
  *  - The fused epilogue of the DeepGEMM kernel-set blog, section 6.1: a bias
  *    per output column, then ReLU or GELU, applied to alpha*(A@B) + beta*C.
  *    GELU is the exact form x * Phi(x) = x/2 * (1 + erf(x / sqrt 2)); ReLU maps
@@ -42,12 +45,39 @@
 #include <omp.h>
 #endif
 
-enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_S4 = 3 };
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_S4 = 3, OR_S8 = 4, OR_E4M3 = 5, OR_E5M2 = 6 };
 
 /* ---- storage formats ---------------------------------------------------- */
 
+/* Exact value of an 8-bit float (the FP8 inputs of the DeepGEMM kernel-set
+ * blog, sections 1.2 and 6.3): sign, ebits exponent bits, mbits mantissa bits.
+ * E4M3 (bias 7) has no infinities; only exponent and mantissa all ones is NaN,
+ * so its largest value is 1.75 * 2^8 = 448.  E5M2 (bias 15) follows IEEE 754:
+ * exponent all ones is infinity (mantissa 0) or NaN.  Exponent 0 holds the
+ * subnormals m * 2^(1 - bias - mbits). */
+static double decode_fp8(int type, uint32_t bits)
+{
+    const int e4 = (type == OR_E4M3);
+    const int mbits = e4 ? 3 : 2, ebits = e4 ? 4 : 5;
+    const int bias = (1 << (ebits - 1)) - 1;
+    const uint32_t sign = (bits >> 7) & 1u;
+    const uint32_t e = (bits >> mbits) & ((1u << ebits) - 1u);
+    const uint32_t m = bits & ((1u << mbits) - 1u);
+    const uint32_t emax = (1u << ebits) - 1u;
+    double v;
+    if (e4 && e == emax && m == (1u << mbits) - 1u)
+        v = NAN;
+    else if (!e4 && e == emax)
+        v = m ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)m, 1 - bias - mbits);
+    else
+        v = ldexp((double)((1u << mbits) + m), (int)e - bias - mbits);
+    return sign ? -v : v;
+}
+
 /* Exact value of a stored fp16 / bf16 / fp32 bit pattern (IEEE 754 binary16,
- * the bfloat16 truncation of binary32, binary32). */
+ * the bfloat16 truncation of binary32, binary32), or of an 8-bit float. */
 double oracle_decode(int type, uint32_t bits)
 {
     if (type == OR_F32) {
@@ -55,6 +85,8 @@ double oracle_decode(int type, uint32_t bits)
         memcpy(&f, &bits, sizeof f);
         return (double)f;
     }
+    if (type == OR_E4M3 || type == OR_E5M2)
+        return decode_fp8(type, bits & 0xFFu);
     int mbits = (type == OR_F16) ? 10 : 7;
     int ebits = (type == OR_F16) ? 5 : 8;
     int bias = (1 << (ebits - 1)) - 1;
@@ -138,9 +170,9 @@ double oracle_ulp(int type, double x)
 
 typedef struct {
     int64_t M, N, K;
-    int a_type;                 /* OR_F16 / OR_BF16                              */
+    int a_type;                 /* OR_F16 / OR_BF16 / OR_E4M3 / OR_E5M2          */
     const void* A; int64_t lda; /* M x K row-major, lda in elements              */
-    int b_type;                 /* OR_F16 / OR_BF16 / OR_S4                      */
+    int b_type;                 /* OR_F16 / OR_BF16 / OR_S4 / OR_E4M3 / OR_E5M2  */
     const void* B; int64_t ldb; /* N x K, K contiguous; S4: bytes per row        */
     int u_type; const void* U; int64_t ldu; int64_t ga; /* [K/ga][M] or U == 0  */
     int v_type; const void* V; int64_t ldv; int64_t gb; /* [K/gb][N] or V == 0  */
@@ -154,6 +186,8 @@ static uint32_t load_bits(int type, const void* p, int64_t idx)
 {
     if (type == OR_F32)
         return ((const uint32_t*)p)[idx];
+    if (type == OR_E4M3 || type == OR_E5M2)
+        return ((const uint8_t*)p)[idx];
     return ((const uint16_t*)p)[idx];
 }
 

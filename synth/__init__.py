@@ -6,8 +6,8 @@ holds none of the GEMM arithmetic, so both the CUDA path and the CPU oracle
 can consume its output without sharing any of the method's code.
 
 Every array is returned as raw storage bits in numpy (uint16 for 16-bit
-floats, uint8 for packed int4, float32 for fp32), laid out exactly as the
-library expects them:
+floats, uint8 for packed int4 and for 8-bit floats, float32 for fp32), laid
+out exactly as the library expects them:
 
 * A   : M x K, row-major (K contiguous)
 * B   : "col-major K x N", i.e. stored N x K with K contiguous
@@ -41,6 +41,11 @@ def _round_bits(x: np.ndarray, dtype: int) -> np.ndarray:
         return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     if dtype == F32:
         return np.ascontiguousarray(x, dtype=np.float32)
+    if dtype in (E4M3, E5M2):
+        # 8-bit floats: RN-even; the workloads' values stay far inside the
+        # finite range (|x| <= 448 for E4M3), so nothing saturates
+        f8 = torch.float8_e4m3fn if dtype == E4M3 else torch.float8_e5m2
+        return t.to(f8).view(torch.uint8).numpy().copy()
     raise ValueError(f"cannot round to dtype {dtype}")
 
 
@@ -129,6 +134,14 @@ def config3(M, seed=1003, N=4096, K=14336) -> Problem:
     """Decode-shaped bf16: M in {1,16,64}, N 4096, K 14336, N(0, 0.02^2), bf16 D."""
     return dense(M, N, K, seed=seed + M, a_type=BF16, d_type=BF16, dist="normal", scale=0.02,
                  name=f"C3 decode M={M}")
+
+
+def config2_fp8(seed=1002, M=4096, N=4096, K=4096, a_type=E4M3) -> Problem:
+    """The dense 4096^3 workload with 8-bit float operands: A and B N(0,1) rounded
+    once to E4M3 (or E5M2), C bf16 N(0,1), alpha 1.5/sqrt(K) (the per-tensor
+    scale that the bf16 workload folds into its operands), beta 0.5, bf16 D."""
+    return dense(M, N, K, seed=seed, a_type=a_type, d_type=BF16, dist="normal", scale=1.0,
+                 alpha=1.5 / float(np.sqrt(K)), beta=0.5, name=f"C2-shaped {DTYPE_NAMES[a_type]} {M}x{N}x{K}")
 
 
 def w4a16(M, N, K, *, seed, group=128, a_type=BF16, d_type=BF16, vlo=0.005, vhi=0.02,

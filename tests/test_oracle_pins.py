@@ -434,3 +434,67 @@ def test_batched_block_is_a_bijection():
     assert got == set(itertools.product(range(batch), range(m_num), range(n_num)))
     assert oracle.batched_block(0, m_num, n_num) == (0, 0, 0)
     assert oracle.batched_block(16, m_num, n_num) == (1, 0, 1)
+
+
+# ---- 8-bit float operands (DeepGEMM kernel-set blog, sections 1.2 and 6.3) ----
+
+def lib_decode_fp8(dtype, bits):
+    f8 = torch.float8_e4m3fn if dtype == oracle.E4M3 else torch.float8_e5m2
+    t = torch.from_numpy(np.asarray(bits, dtype=np.uint8).copy()).view(f8)
+    return t.to(torch.float64).numpy()
+
+
+@pytest.mark.parametrize("dtype", [oracle.E4M3, oracle.E5M2])
+def test_fp8_decode_every_pattern(dtype):
+    bits = np.arange(256, dtype=np.uint32)
+    got = oracle.decode(dtype, bits)
+    want = lib_decode_fp8(dtype, bits.astype(np.uint8))
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert math.copysign(1.0, got[0x80]) == -1.0
+
+
+def test_fp8_format_closed_forms():
+    # values fixed by the two formats' definitions (sign, exponent with bias 7
+    # or 15, 3 or 2 mantissa bits; E4M3 keeps only all-ones as NaN and has no
+    # infinity; E5M2 has IEEE infinities and NaNs)
+    e4 = {0x38: 1.0, 0x7E: 448.0, 0x08: 2.0 ** -6, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0xC4: -3.0,
+          0x77: 240.0, 0x78: 256.0}
+    e5 = {0x3C: 1.0, 0x7B: 57344.0, 0x04: 2.0 ** -14, 0x01: 2.0 ** -16, 0x03: 3 * 2.0 ** -16, 0xC2: -3.0,
+          0x7C: math.inf, 0xFC: -math.inf}
+    for bits, v in e4.items():
+        assert oracle.decode(oracle.E4M3, [bits])[0] == v, hex(bits)
+    for bits, v in e5.items():
+        assert oracle.decode(oracle.E5M2, [bits])[0] == v, hex(bits)
+    assert np.isnan(oracle.decode(oracle.E4M3, [0x7F, 0xFF])).all()
+    assert not np.isnan(oracle.decode(oracle.E4M3, [0x7C, 0x7D, 0x7E])).any()  # exponent all ones, finite
+    assert np.isnan(oracle.decode(oracle.E5M2, [0x7D, 0x7E, 0x7F, 0xFF])).all()
+
+
+@pytest.mark.parametrize("dtype", [oracle.E4M3, oracle.E5M2])
+def test_fp8_dense_matches_numpy_matmul(dtype):
+    rng = random.Random(31 + dtype)
+    for case in range(12):
+        M, N, K = (rng.randint(1, 40) for _ in range(3))
+        beta = rng.choice([0.0, 0.5])
+        p = synth.dense(M, N, K, seed=200 + case, a_type=dtype, d_type=BF16, dist="normal",
+                        alpha=rng.choice([1.0, 0.03125, -0.75]), beta=beta)
+        ref, bound = oracle.gemm(p)
+        a, b = lib_decode_fp8(dtype, p.A), lib_decode_fp8(dtype, p.B)
+        want = p.alpha * (a @ b.T)
+        wb = abs(p.alpha) * (np.abs(a) @ np.abs(b.T))
+        if beta != 0.0:
+            c = lib_decode(BF16, p.C)
+            want, wb = want + beta * c, wb + np.abs(beta * c)
+        np.testing.assert_allclose(ref, want, rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(bound, wb, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("dtype,one", [(oracle.E4M3, 0x38), (oracle.E5M2, 0x3C)])
+def test_fp8_identity_b_closed_form(dtype, one):
+    K = 40
+    p = synth.dense(9, K, K, seed=5, a_type=dtype, d_type=BF16, dist="normal", alpha=1.5, beta=0.5)
+    p.B = np.where(np.eye(K, dtype=bool), np.uint8(one), np.uint8(0)).astype(np.uint8)
+    ref, _ = oracle.gemm(p)
+    assert np.array_equal(ref, 1.5 * lib_decode_fp8(dtype, p.A) + 0.5 * lib_decode(BF16, p.C))
