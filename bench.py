@@ -8,7 +8,7 @@ TFLOP/s = 2*M*N*K / time.  Three rotating input sets (384 MB) keep the
 operands out of the 129 MB L2 between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config c2|c1|c3m1|c3m16|c3m64|c4|c5]
+                    [--config c2|c1|c3m1|c3m16|c3m64|c4|c5|c2f8]
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the GEMM has no exchange step), timing is the max over ranks and the value
@@ -71,6 +71,8 @@ WORKLOADS = {
     "c4": dict(desc="W4A16 GEMM M=128 K=4096 N=11008, int4 B + fp16 group-128 scales, bf16 D", kind="dense"),
     "c5": dict(desc="grouped MoE bf16 GEMM, 8 experts, 4096 tokens Zipf(1.2), K=4096, N=14336, bf16 D",
                kind="grouped"),
+    "c2f8": dict(desc="dense E4M3 GEMM M=N=K=4096, A row-major, B col-major, N(0,1) rounded to E4M3, C bf16 "
+                      "N(0,1), alpha 1.5/64 beta 0.5, bf16 D", kind="dense"),
 }
 
 
@@ -99,6 +101,8 @@ def make_problem(cfg):
         return synth.config4()
     if cfg == "c5":
         return synth.config5()
+    if cfg == "c2f8":
+        return synth.config2_fp8()
     raise ValueError(cfg)
 
 
@@ -115,8 +119,9 @@ def algorithmic_bytes(p):
         experts = int((p.counts > 0).sum())
         return 2 * (T * p.K + experts * p.N * p.K + T * p.N)
     out_b = 4 if p.d_type == synth.F32 else 2
-    b = 2 * p.M * p.K + out_b * p.M * p.N
-    b += p.N * p.K // 2 if p.b_type == synth.S4 else 2 * p.N * p.K
+    in_b = 1 if p.a_type in (synth.E4M3, synth.E5M2) else 2
+    b = in_b * p.M * p.K + out_b * p.M * p.N
+    b += p.N * p.K // 2 if p.b_type == synth.S4 else in_b * p.N * p.K
     if p.V is not None:
         b += p.V.size * (4 if p.v_type == synth.F32 else 2)
     if p.beta != 0.0:
@@ -255,6 +260,9 @@ class Runner:
             return torch.from_numpy(np.ascontiguousarray(bits)).cuda()
         if dtype == synth.F32:
             return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.float32)).cuda()
+        if dtype in (synth.E4M3, synth.E5M2):
+            f8 = torch.float8_e4m3fn if dtype == synth.E4M3 else torch.float8_e5m2
+            return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint8)).view(f8).cuda()
         t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
         return t.view(torch.bfloat16 if dtype == synth.BF16 else torch.float16).cuda()
 
@@ -392,7 +400,7 @@ SCHEDULES = {"auto": (0, 0), "unsplit": (1, 0), "splitk8": (8, 0), "streamk": (0
 # automatic choice.
 SUB_CONFIGS = ([("c1", "auto")] +
                [(f"c3m{m}", s) for m in (1, 16, 64) for s in ("auto", "unsplit", "splitk8", "streamk")] +
-               [("c4", "auto"), ("c5", "auto")])
+               [("c4", "auto"), ("c5", "auto"), ("c2f8", "auto")])
 
 
 def measure_config(cfg, sched, steps, warmup, launch, sampler, peaks, peak_src, qg, torch, p=None):

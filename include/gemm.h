@@ -51,7 +51,12 @@ typedef enum {
 } gemm_status_t;
 
 /* ---- operand description ------------------------------------------------------ */
-typedef enum { GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2, GEMM_S4 = 3, GEMM_S8 = 4 } gemm_dtype_t;
+typedef enum {
+    GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2,
+    GEMM_S4 = 3,                /* two's-complement nibbles, two per byte        */
+    GEMM_S8 = 4,                /* int8 (quantised D)                           */
+    GEMM_E4M3 = 5, GEMM_E5M2 = 6 /* 8-bit floats (1-4-3 bias 7, no infinity; 1-5-2 bias 15) */
+} gemm_dtype_t;
 typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_order_t;
 
 /*
@@ -63,12 +68,14 @@ typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_order_t;
  * grouped GEMM).
  *
  * Operands served (anything else returns GEMM_ERR_UNSUPPORTED):
- *   A : M x K, row-major, f16/bf16                 (K contiguous)
- *   B : K x N, col-major, same type as A, or S4     (K contiguous)
+ *   A : M x K, row-major, f16/bf16/e4m3/e5m2        (K contiguous)
+ *   B : K x N, col-major, same type as A, or S4 with a 16-bit A (K contiguous)
  *   U : (K/ga) x M, row-major, f16/bf16            scale of A per (row, K-group)
  *   V : (K/gb) x N, row-major, f16/bf16            scale of B per (K-group, column)
  *   C : M x N, row-major, same type as D
  *   D : M x N, row-major, f32/f16/bf16
+ * 8-bit float operands (the FP8 inputs of the DeepGEMM kernel-set blog,
+ * sections 1.2 and 6.3) take no U/V: a per-tensor scale goes into alpha.
  * A, B, U and V base addresses must be 16-byte aligned and their ld a
  * multiple of 16 bytes (they are read by the tensor-memory accelerator); C
  * and D may have any ld >= N and element alignment (16-byte aligned ones are
@@ -173,6 +180,7 @@ int gemm_destroy(gemm_handle_t h);
 
 /*
  * Gemm::Run.  D = alpha * (A-hat @ B-hat) + beta * C.
+ * With fp16/bf16 or E4M3/E5M2 operands every product is exact in fp32.
  *   A-hat[i][k] = A[i][k], or RN_A(A[i][k] * U[k/ga][i]) with U;
  *   B-hat[k][j] = B[k][j], or RN_B(B[k][j] * V[k/gb][j]) with V;
  *   int4 B: B-hat[k][j] = RN_A(q[k][j] * V[k/gb][j]) (q without V), where q

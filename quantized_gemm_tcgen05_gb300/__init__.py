@@ -26,7 +26,7 @@ GEMM_ERR_NO_KERNEL = 5
 GEMM_ERR_DEVICE_TIMEOUT = 6
 GEMM_ERR_BAD_CACHE = 7
 
-GEMM_F32, GEMM_F16, GEMM_BF16, GEMM_S4, GEMM_S8 = 0, 1, 2, 3, 4
+GEMM_F32, GEMM_F16, GEMM_BF16, GEMM_S4, GEMM_S8, GEMM_E4M3, GEMM_E5M2 = 0, 1, 2, 3, 4, 5, 6
 GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
 GEMM_DISPATCH_DEFAULT, GEMM_DISPATCH_MEASURE, GEMM_DISPATCH_REUSE = 0, 1, 2
 GEMM_EPILOGUE_DEFAULT, GEMM_EPILOGUE_BIAS, GEMM_EPILOGUE_RELU, GEMM_EPILOGUE_GELU = 0, 1, 2, 4
@@ -240,7 +240,8 @@ def gemm_grouped_block(sizes, block_m, block):
 
 def _dtype_code(t):
     import torch
-    return {torch.float32: GEMM_F32, torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16, torch.int8: GEMM_S8}[t]
+    return {torch.float32: GEMM_F32, torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16, torch.int8: GEMM_S8,
+            torch.float8_e4m3fn: GEMM_E4M3, torch.float8_e5m2: GEMM_E5M2}[t]
 
 
 def layout(type_, order, rows, cols, ld, num=1, batch_stride=0):

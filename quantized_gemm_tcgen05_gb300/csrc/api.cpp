@@ -53,14 +53,21 @@ struct gemm_handle {
 namespace {
 
 bool is16(int32_t t) { return t == GEMM_F16 || t == GEMM_BF16; }
+bool is_f8(int32_t t) { return t == GEMM_E4M3 || t == GEMM_E5M2; }
+// Bytes per element of a tensor-core input (16-bit or 8-bit float).
+int64_t in_bytes(int32_t t) { return is_f8(t) ? 1 : 2; }
+// Tensor-map element type of a tensor-core input.
+CUtensorMapDataType in_map_type(int32_t t) {
+    if (is_f8(t)) return CU_TENSOR_MAP_DATA_TYPE_UINT8;  // raw bytes: TMA only moves them
+    return t == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
 bool is_float_out(int32_t t) { return t == GEMM_F32 || t == GEMM_F16 || t == GEMM_BF16; }
 static_assert(GEMM_F32 == DT_F32 && GEMM_F16 == DT_F16 && GEMM_BF16 == DT_BF16 && GEMM_S4 == DT_S4 &&
-                  GEMM_S8 == DT_S8,
+                  GEMM_S8 == DT_S8 && GEMM_E4M3 == DT_E4M3 && GEMM_E5M2 == DT_E5M2,
               "the C ABI's dtype codes are the kernels' codes");
 static_assert(GEMM_EPILOGUE_BIAS == EPI_BIAS && GEMM_EPILOGUE_RELU == EPI_RELU && GEMM_EPILOGUE_GELU == EPI_GELU,
               "the C ABI's epilogue flags are the kernels' flags");
 
-int64_t elem_bytes_x2(int32_t t) { return t == GEMM_F32 ? 8 : (t == GEMM_S4 ? 1 : 4); }  // 2 * bytes
 
 bool device_pointer_uncached(const void* p) {
     cudaPointerAttributes a;
@@ -197,40 +204,44 @@ int gemm_destroy(gemm_handle_t h) {
 
 namespace {
 
-// Tensor map over a [batches][rows][K] operand stored with K contiguous.
+// Tensor map over a [batches][rows][K] operand stored with K contiguous; a
+// box is one K-step (128 bytes) of box_rows rows.
 int make_map(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t type, int64_t K, int64_t rows, int64_t ld,
              int32_t batches, int64_t bstride, int32_t box_rows) {
-    CUtensorMapDataType dt = type == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapDataType dt = in_map_type(type);
+    const int64_t es = in_bytes(type);
     cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)batches};
-    cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)bstride * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld * es), (cuuint64_t)(bstride * es)};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / es), (cuuint32_t)box_rows, 1};
     const cuuint32_t rank = batches > 1 ? 3 : 2;
     CUresult r = encode_cached(h, m, dt, rank, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-// Tensor map over a 16-bit K-major operand viewed as [K/64 chunks][rows][64]:
-// a box of two 64-wide chunks x box_rows rows lands as two SWIZZLE_128B
-// tiles, one copy for two K-steps.  Only for K a multiple of 64 (the 64-wide
-// inner dimension must not run past a row).
+// Tensor map over a K-major operand viewed as [K-steps][rows][one K-step of
+// 128 bytes]: a box of several K-steps x box_rows rows lands as that many
+// SWIZZLE_128B tiles, one copy for several K-steps.  Only for K a multiple of
+// the K-step (the inner dimension must not run past a row).
 int make_map_kchunk(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t type, int64_t K, int64_t rows, int64_t ld,
                     int32_t box_rows, int32_t chunks) {
-    CUtensorMapDataType dt = type == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(K / 64)};
-    cuuint64_t strides[2] = {(cuuint64_t)ld * 2, 128};
-    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)chunks};
+    const CUtensorMapDataType dt = in_map_type(type);
+    const int64_t es = in_bytes(type), kstep = 128 / es;
+    cuuint64_t dims[3] = {(cuuint64_t)kstep, (cuuint64_t)rows, (cuuint64_t)(K / kstep)};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld * es), 128};
+    cuuint32_t box[3] = {(cuuint32_t)kstep, (cuuint32_t)box_rows, (cuuint32_t)chunks};
     CUresult r = encode_cached(h, m, dt, 3, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 // The same K-chunk view over a [batches][rows][K] operand (grouped experts):
-// [batches][K/64][rows][64], one expert per box.
+// [batches][K-steps][rows][one K-step], one expert per box.
 int make_map_kchunk4(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t type, int64_t K, int64_t rows,
                      int64_t ld, int32_t batches, int64_t bstride, int32_t box_rows, int32_t chunks) {
-    CUtensorMapDataType dt = type == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)(K / 64), (cuuint64_t)batches};
-    cuuint64_t strides[3] = {(cuuint64_t)ld * 2, 128, (cuuint64_t)bstride * 2};
-    cuuint32_t box[4] = {64, (cuuint32_t)box_rows, (cuuint32_t)chunks, 1};
+    const CUtensorMapDataType dt = in_map_type(type);
+    const int64_t es = in_bytes(type), kstep = 128 / es;
+    cuuint64_t dims[4] = {(cuuint64_t)kstep, (cuuint64_t)rows, (cuuint64_t)(K / kstep), (cuuint64_t)batches};
+    cuuint64_t strides[3] = {(cuuint64_t)(ld * es), 128, (cuuint64_t)(bstride * es)};
+    cuuint32_t box[4] = {(cuuint32_t)kstep, (cuuint32_t)box_rows, (cuuint32_t)chunks, 1};
     CUresult r = encode_cached(h, m, dt, 4, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -298,7 +309,7 @@ int pair_kchunks(const Problem& p) {
         const int v = e ? atoi(e) : 2;
         return v >= 1 && v <= 3 ? v : 2;
     }();
-    if (want < 2 || p.K % 64 != 0 || p.batches != 1 || p.K < 64) return 1;
+    if (want < 2 || p.K % kstep_of(p) != 0 || p.batches != 1 || p.K < kstep_of(p)) return 1;
     return want;
 }
 
@@ -311,7 +322,7 @@ int single_kchunks(const Problem& p, const Choice& c) {
         const int v = e ? atoi(e) : 2;
         return v >= 1 && v <= 3 ? v : 2;
     }();
-    if (p.K % 64 != 0 || p.batches != 1 || p.K < 64 || p.family != FAM_DENSE) return 1;
+    if (p.K % kstep_of(p) != 0 || p.batches != 1 || p.K < kstep_of(p) || p.family != FAM_DENSE) return 1;
     for (int ks = want; ks > 1; --ks)
         if (umma_max_stages(c.bn, ks) >= 3) return ks;
     return 1;
@@ -395,7 +406,10 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
     e.vec_ok = aligned16(p.D) && (p.ldd * eb) % 16 == 0 &&
                (e.C == nullptr || (aligned16(p.C) && (p.ldc * eb) % 16 == 0)) &&
                (p.batches == 1 || ((p.d_bs * eb) % 16 == 0 && (e.C == nullptr || (p.c_bs * eb) % 16 == 0)));
-    kp.idesc = make_idesc_f16(p.a_type == GEMM_BF16, 128, c.bn);
+    kp.mma_f8 = is_f8(p.a_type);
+    kp.kstep = kstep_of(p);
+    kp.idesc = kp.mma_f8 ? make_idesc_f8(p.a_type == GEMM_E5M2, p.b_type == GEMM_E5M2, 128, c.bn)
+                         : make_idesc_f16(p.a_type == GEMM_BF16, 128, c.bn);
     kp.status = h->status;
     kp.timeout_ns = h->timeout_ns;
 
@@ -520,7 +534,8 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
     }
     if (c.pair) {
         kp.pair = 1;
-        kp.idesc = make_idesc_f16(p.a_type == GEMM_BF16, 256, c.bn);
+        kp.idesc = kp.mma_f8 ? make_idesc_f8(p.a_type == GEMM_E5M2, p.b_type == GEMM_E5M2, 256, c.bn)
+                             : make_idesc_f16(p.a_type == GEMM_BF16, 256, c.bn);
         cudaError_t ce = launch_umma_pair_gemm(c.bn, maps, kp, 2 * kp.sched.programs, st);
         return ce == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
@@ -757,8 +772,10 @@ int build_problem(gemm_handle* h, const gemm_op_t* op, float alpha, const void* 
     p.a_type = Adesc->type;
     p.b_type = Bdesc->type;
     p.d_type = Ddesc->type;
-    if (!is16(p.a_type)) return GEMM_ERR_UNSUPPORTED;
-    if (!(p.b_type == p.a_type || p.b_type == GEMM_S4)) return GEMM_ERR_UNSUPPORTED;
+    // A and B: both f16, both bf16, both E4M3 or both E5M2; or 16-bit A with int4 B
+    if (!is16(p.a_type) && !is_f8(p.a_type)) return GEMM_ERR_UNSUPPORTED;
+    if (!(p.b_type == p.a_type || (p.b_type == GEMM_S4 && is16(p.a_type)))) return GEMM_ERR_UNSUPPORTED;
+    p.kstep = (int32_t)(128 / in_bytes(p.a_type));
     if (!is_float_out(p.d_type) && p.d_type != GEMM_S8) return GEMM_ERR_UNSUPPORTED;
     int rc;
     if ((rc = check_layout(Adesc, GEMM_ROW_MAJOR, p.M, p.K))) return rc;
@@ -822,6 +839,7 @@ int build_problem(gemm_handle* h, const gemm_op_t* op, float alpha, const void* 
         p.v_type = Vdesc->type;
     }
     p.family = (p.U || p.V || p.b_type == GEMM_S4) ? FAM_DQ : FAM_DENSE;
+    if (is_f8(p.a_type) && p.family != FAM_DENSE) return GEMM_ERR_UNSUPPORTED;  // no U/V on 8-bit operands
     if (grouped) {
         if (p.U || p.V || p.b_type == GEMM_S4) return GEMM_ERR_UNSUPPORTED;
         if (Adesc->num != 1 || Ddesc->num != 1) return GEMM_ERR_INVALID_ARG;
@@ -843,17 +861,17 @@ int build_problem(gemm_handle* h, const gemm_op_t* op, float alpha, const void* 
     if (p.K > 0) {
         // operands read by the tensor-memory accelerator
         if (!aligned16(A) || !aligned16(B)) return GEMM_ERR_INVALID_ARG;
-        if ((p.lda * 2) % 16 || (p.a_bs * 2) % 16) return GEMM_ERR_INVALID_ARG;
+        const int64_t es = in_bytes(p.a_type);
+        if ((p.lda * es) % 16 || (p.a_bs * es) % 16) return GEMM_ERR_INVALID_ARG;
         if (p.b_type == GEMM_S4) {
             if (p.K % 2 || p.ldb % 32) return GEMM_ERR_INVALID_ARG;
-        } else if ((p.ldb * 2) % 16 || (p.b_bs * 2) % 16) {
+        } else if ((p.ldb * es) % 16 || (p.b_bs * es) % 16) {
             return GEMM_ERR_INVALID_ARG;
         }
         if (!device_pointer(h, A) || !device_pointer(h, B)) return GEMM_ERR_INVALID_ARG;
     }
     if (!device_pointer(h, D)) return GEMM_ERR_INVALID_ARG;
     if (p.C && !device_pointer(h, p.C)) return GEMM_ERR_INVALID_ARG;
-    (void)elem_bytes_x2;
     *out = p;
     return GEMM_OK;
 }
@@ -999,7 +1017,8 @@ int gemm_heuristic_choice(int64_t m, int64_t n, int64_t k, int32_t a_type, int32
                           int32_t quant_a_group, int32_t quant_b_group, int32_t num_experts, int32_t sm_count,
                           size_t partials_size, char* out, size_t cap) {
     if (!out || cap == 0 || m < 1 || n < 1 || k < 1 || sm_count < 1 || num_experts < 0) return GEMM_ERR_INVALID_ARG;
-    if (!is16(a_type) || !(b_type == a_type || b_type == GEMM_S4)) return GEMM_ERR_INVALID_ARG;
+    if ((!is16(a_type) && !is_f8(a_type)) || !(b_type == a_type || (b_type == GEMM_S4 && is16(a_type))))
+        return GEMM_ERR_INVALID_ARG;
     if (!is_float_out(d_type) && d_type != GEMM_S8) return GEMM_ERR_INVALID_ARG;
     Problem p;
     memset(&p, 0, sizeof p);
@@ -1009,7 +1028,9 @@ int gemm_heuristic_choice(int64_t m, int64_t n, int64_t k, int32_t a_type, int32
     p.a_type = a_type;
     p.b_type = b_type;
     p.d_type = d_type;
+    p.kstep = (int32_t)(128 / in_bytes(a_type));
     p.batches = 1;
+    if (is_f8(a_type) && (quant_a_group > 0 || quant_b_group > 0)) return GEMM_ERR_INVALID_ARG;
     // the heuristic only asks whether scales are present: a marker stands in
     static const int32_t marker = 0;
     if (quant_a_group > 0) {

@@ -50,7 +50,7 @@ Key make_key(const Problem& p) {
 SchedParams make_sched(const Problem& p, const Choice& c, int sm_count) {
     SchedParams s;
     memset(&s, 0, sizeof s);
-    s.k_iters = (int32_t)ceil_div(p.K, BK_HOST);
+    s.k_iters = (int32_t)ceil_div(p.K, kstep_of(p));
     s.batches = p.batches;
     if (p.family == FAM_GROUPED) {
         // upper bound on padded M-blocks: sum_e ceil(m_e / bm) <= T / bm + E
@@ -87,7 +87,7 @@ SchedParams make_sched(const Problem& p, const Choice& c, int sm_count) {
         int64_t iters = T * s.k_iters;
         s.programs = (int32_t)(iters < sm_count ? iters : sm_count);
         StreamKPlan pl = streamk_plan((int64_t)s.tiles_x * 128, (int64_t)s.tiles_y * c.bn * s.batches, p.K, 128,
-                                      c.bn, BK_HOST, s.programs);
+                                      c.bn, kstep_of(p), s.programs);
         s.sk_tiles = (int32_t)pl.streamk_tiles;
         s.sk_full = (int32_t)pl.full_tiles;
         s.sk_partial = (int32_t)pl.partial_tiles;
@@ -125,6 +125,7 @@ static bool swap_allowed(const Problem& p) {
 bool gemv_eligible(const Problem& p) {
     if (p.family != FAM_DENSE && p.family != FAM_DQ) return false;
     if (p.batches != 1 || p.M < 1 || p.M > 8 || p.U != nullptr) return false;
+    if (p.a_type != DT_F16 && p.a_type != DT_BF16) return false;
     return p.K / 8 < (int64_t(1) << 24);
 }
 
@@ -147,7 +148,7 @@ static Choice gemv_choice() {
 std::vector<Choice> candidates(const Problem& p, int sm_count) {
     std::vector<Choice> out;
     if (gemv_eligible(p)) out.push_back(gemv_choice());
-    const int64_t k_iters = ceil_div(p.K, BK_HOST);
+    const int64_t k_iters = ceil_div(p.K, kstep_of(p));
     auto add_scheds = [&](int32_t bn, int32_t swap) {
         Choice c;
         c.bn = bn;

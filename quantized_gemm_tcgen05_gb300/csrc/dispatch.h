@@ -23,6 +23,7 @@ struct Problem {
     int64_t M, N, K;
     int32_t batches;
     int32_t a_type, b_type, d_type;
+    int32_t kstep;                      // elements per K-step: 64 (16-bit operands) or 128 (8-bit)
     const void* A; int64_t lda, a_bs;
     const void* B; int64_t ldb, b_bs;   // stored N x K (K contiguous); S4: ld in nibbles
     const void* U; int64_t ldu; int32_t u_type, ga;
@@ -67,8 +68,11 @@ SchedParams make_sched(const Problem& p, const Choice& c, int sm_count);
 size_t partials_bytes_needed(const SchedParams& s, int bn, int pair);
 size_t counters_bytes_needed(const SchedParams& s, int pair);
 
+// Elements per K-step (one 128-byte swizzle row) of the problem's operands.
+inline int32_t kstep_of(const Problem& p) { return p.kstep > 0 ? p.kstep : BK_HOST; }
+
 // The small-M streaming kernel takes the problem: M <= 8, one batch, no U
-// scale, B 16-bit or int4 (with or without V).
+// scale, A 16-bit, B 16-bit or int4 (with or without V).
 bool gemv_eligible(const Problem& p);
 
 // Every kernel variant that can run the problem.

@@ -10,7 +10,7 @@
 
 namespace qg {
 
-enum DType : int32_t { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2, DT_S4 = 3, DT_S8 = 4 };
+enum DType : int32_t { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2, DT_S4 = 3, DT_S8 = 4, DT_E4M3 = 5, DT_E5M2 = 6 };
 
 // Where a bounded wait gave up (recorded in the device status word).
 enum WaitSite : uint32_t {
@@ -82,7 +82,9 @@ struct GemmKernelParams {
     uint32_t* status;     // device status words [4]
     uint64_t timeout_ns;  // bound on every wait
     int32_t pair;         // CTA-pair kernel: units are 256-row tiles shared by the two CTAs of a cluster
-    int32_t ks;           // 64-wide K-steps per stage (>1: X/Y maps index 64-wide K chunks)
+    int32_t ks;           // K-steps per stage (>1: X/Y maps index K chunks of one K-step)
+    int32_t kstep;        // elements per K-step: one 128-byte swizzle row (64 16-bit, 128 8-bit values)
+    int32_t mma_f8;       // operands are 8-bit floats: tcgen05.mma.kind::f8f6f4
 };
 
 // Instruction descriptor of tcgen05.mma.kind::f16: fp32 accumulator (bits
@@ -91,6 +93,13 @@ struct GemmKernelParams {
 QG_HD uint32_t make_idesc_f16(int ab_is_bf16, int m, int n) {
     uint32_t fmt = ab_is_bf16 ? 1u : 0u;
     return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+// Instruction descriptor of tcgen05.mma.kind::f8f6f4: the same fields, with
+// the A/B formats E4M3 = 0 and E5M2 = 1.
+QG_HD uint32_t make_idesc_f8(int a_e5m2, int b_e5m2, int m, int n) {
+    return (1u << 4) | ((uint32_t)(a_e5m2 ? 1 : 0) << 7) | ((uint32_t)(b_e5m2 ? 1 : 0) << 10) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 // Tile widths (UMMA N) instantiated for each kernel.

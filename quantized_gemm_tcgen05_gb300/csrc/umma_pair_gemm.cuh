@@ -172,23 +172,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     } else if (leader) {
                         mbar_arrive_expect_tx(&full[s], 2 * (Cfg::A_BYTES + Cfg::B_BYTES));
                         if (P.x3d)
-                            tma_load_3d(a, &tmX, &full[s], k * BK, (int32_t)u.x_row0, u.batch);
+                            tma_load_3d(a, &tmX, &full[s], k * P.kstep, (int32_t)u.x_row0, u.batch);
                         else
-                            tma_load_2d(a, &tmX, &full[s], k * BK, (int32_t)u.x_row0);
+                            tma_load_2d(a, &tmX, &full[s], k * P.kstep, (int32_t)u.x_row0);
                         if (P.y3d)
-                            tma_load_3d(b, &tmY, &full[s], k * BK, y0, u.batch);
+                            tma_load_3d(b, &tmY, &full[s], k * P.kstep, y0, u.batch);
                         else
-                            tma_load_2d(b, &tmY, &full[s], k * BK, y0);
+                            tma_load_2d(b, &tmY, &full[s], k * P.kstep, y0);
                     } else {
                         const uint32_t lf = mapa_shared(smem_u32(&full[s]), 0);
                         if (P.x3d)
-                            tma_load_3d_pair(a, &tmX, lf, k * BK, (int32_t)u.x_row0, u.batch);
+                            tma_load_3d_pair(a, &tmX, lf, k * P.kstep, (int32_t)u.x_row0, u.batch);
                         else
-                            tma_load_2d_pair(a, &tmX, lf, k * BK, (int32_t)u.x_row0);
+                            tma_load_2d_pair(a, &tmX, lf, k * P.kstep, (int32_t)u.x_row0);
                         if (P.y3d)
-                            tma_load_3d_pair(b, &tmY, lf, k * BK, y0, u.batch);
+                            tma_load_3d_pair(b, &tmY, lf, k * P.kstep, y0, u.batch);
                         else
-                            tma_load_2d_pair(b, &tmY, lf, k * BK, y0);
+                            tma_load_2d_pair(b, &tmY, lf, k * P.kstep, y0);
                     }
                     armed |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
@@ -238,10 +238,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     for (int h = 0; h < nk; ++h) {
                         const uint64_t ad = make_sw128_kmajor_desc(a_addr + h * Cfg::A_BYTES);
                         const uint64_t bd = make_sw128_kmajor_desc(a_addr + a_region + h * Cfg::B_BYTES);
+                        // four instructions per K-step, 32 bytes of each operand row apiece
+                        if (P.mma_f8) {
 #pragma unroll
-                        for (int kk = 0; kk < BK / UMMA_K; ++kk)
-                            umma_f16_ss_pair(d, ad + 2 * kk, bd + 2 * kk, P.idesc,
-                                             (k + h > u.k_begin || kk > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < 4; ++kk)
+                                umma_f8_ss_pair(d, ad + 2 * kk, bd + 2 * kk, P.idesc,
+                                                (k + h > u.k_begin || kk > 0) ? 1u : 0u);
+                        } else {
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                umma_f16_ss_pair(d, ad + 2 * kk, bd + 2 * kk, P.idesc,
+                                                 (k + h > u.k_begin || kk > 0) ? 1u : 0u);
+                        }
                     }
                     issued = true;
                     umma_commit_pair_mc(&empty[s], 0x3);

@@ -27,7 +27,8 @@
 
 namespace qg {
 
-// K-steps are 64 elements wide: one 128-byte swizzle row of 16-bit values.
+// A K-step is one 128-byte swizzle row of each operand: 64 16-bit values
+// (the default), or 128 8-bit ones.
 constexpr int32_t BK_HOST = 64;
 
 enum SchedKind : int32_t { SCHED_DP = 0, SCHED_SPLITK = 1, SCHED_STREAMK = 2 };

@@ -19,7 +19,8 @@ import quantized_gemm_tcgen05_gb300 as qg
 import oracle
 import synth
 
-TORCH_DT = {synth.F32: torch.float32, synth.F16: torch.float16, synth.BF16: torch.bfloat16, synth.S8: torch.int8}
+TORCH_DT = {synth.F32: torch.float32, synth.F16: torch.float16, synth.BF16: torch.bfloat16, synth.S8: torch.int8,
+            synth.E4M3: torch.float8_e4m3fn, synth.E5M2: torch.float8_e5m2}
 
 
 def dev_bits(bits, dtype):
@@ -28,6 +29,8 @@ def dev_bits(bits, dtype):
         return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.float32)).cuda()
     if dtype == synth.S4:
         return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint8)).cuda()
+    if dtype in (synth.E4M3, synth.E5M2):
+        return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint8)).view(TORCH_DT[dtype]).cuda()
     t = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16))
     return t.view(TORCH_DT[dtype]).cuda()
 

@@ -95,7 +95,7 @@ def test_binding_struct_layouts_match_the_header(tmp_path):
         lines.append(f'printf("{name} size %zu\\n", sizeof({name}));')
         for field, _ in cls._fields_:
             lines.append(f'printf("{name}.{field} %zu\\n", offsetof({name}, {field}));')
-    consts = ["GEMM_F32", "GEMM_F16", "GEMM_BF16", "GEMM_S4", "GEMM_S8", "GEMM_EPILOGUE_BIAS", "GEMM_EPILOGUE_RELU",
+    consts = ["GEMM_F32", "GEMM_F16", "GEMM_BF16", "GEMM_S4", "GEMM_S8", "GEMM_E4M3", "GEMM_E5M2", "GEMM_EPILOGUE_BIAS", "GEMM_EPILOGUE_RELU",
               "GEMM_EPILOGUE_GELU", "GEMM_DISPATCH_MEASURE", "GEMM_BARRIERS_SIZE", "GEMM_PARTIALS_SIZE",
               "GEMM_NOALLOC_BARRIERS_SIZE", "GEMM_NOALLOC_PARTIALS_SIZE"]
     lines += [f'printf("{c} %d\\n", (int){c});' for c in consts]

@@ -98,3 +98,28 @@ def test_pair_kernel_config2_full_sampled(lib, monkeypatch):
     ii, jj = sample_indices(p.M, p.N, 2000, seed=8)
     ref, bound = oracle.gemm_entries(p, ii, jj)
     assert_close(D.double().cpu().numpy()[ii, jj], ref, bound, p.d_type, "pair C2 sampled")
+
+
+def test_pair_kernel_many_waves_elementwise(lib, monkeypatch):
+    # 10 x 11 = 110 tiles of 256 x 224 on at most 76 clusters: every cluster
+    # reuses both TMEM accumulators and turns its ring phases over, checked
+    # element by element
+    monkeypatch.setenv("GEMM_FORCE_KERNEL", "umma2_bn224/dp")
+    p = synth.dense(2560, 2304, 64, seed=2560, a_type=synth.BF16, d_type=synth.BF16, alpha=1.5, beta=0.5,
+                    dist="normal", scale=0.25)
+    rc, D = run_problem(lib, p)
+    assert rc == 0, qg.gemm_status_string(rc)
+    ref, bound = oracle.gemm(p)
+    assert_close(D.double().cpu().numpy(), ref, bound, p.d_type, "pair, many waves")
+
+
+def test_pair_grouped_many_waves_elementwise(lib, monkeypatch):
+    # 17 expert blocks of 256 rows x 8 column tiles = 136 pair tiles
+    from gpu_helpers import run_grouped
+    monkeypatch.setenv("GEMM_FORCE_KERNEL", "umma2_grouped_bn256/dp")
+    gp = synth.grouped([1000, 0, 1500, 700, 900], 2048, 128, seed=4100)
+    rc, D = run_grouped(lib, gp)
+    assert rc == 0, qg.gemm_status_string(rc)
+    assert qg.gemm_last_choice(lib.h) == "umma2_grouped_bn256/dp"
+    ref, bound = oracle.grouped(gp)
+    assert_close(D.double().cpu().numpy(), ref, bound, gp.d_type, "pair grouped, many waves")
