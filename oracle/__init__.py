@@ -62,6 +62,7 @@ class _Gemm(ctypes.Structure):
         ("c_type", ctypes.c_int), ("C", ctypes.c_void_p), ("ldc", ctypes.c_int64),
         ("alpha", ctypes.c_double), ("beta", ctypes.c_double),
         ("epilogue", ctypes.c_int), ("bias_type", ctypes.c_int), ("bias", ctypes.c_void_p),
+        ("Z", ctypes.c_void_p), ("ldz", ctypes.c_int64),
     ]
 
 
@@ -78,6 +79,8 @@ def lib():
             L.oracle_ulp.argtypes = [ctypes.c_int, ctypes.c_double]
             L.oracle_int4_at.restype = ctypes.c_int
             L.oracle_int4_at.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
+            L.oracle_zero_at.restype = ctypes.c_int
+            L.oracle_zero_at.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
             L.oracle_gemm.restype = ctypes.c_int
             L.oracle_gemm.argtypes = [ctypes.POINTER(_Gemm), ctypes.c_void_p, ctypes.c_void_p]
             L.oracle_gemm_entries.restype = ctypes.c_int
@@ -120,6 +123,13 @@ def ulp(dtype: int, values) -> np.ndarray:
 def int4_at(packed: np.ndarray, n: int, k: int) -> int:
     p = np.ascontiguousarray(packed, dtype=np.uint8)
     return int(lib().oracle_int4_at(p.ctypes.data, p.shape[1], n, k))
+
+
+def zero_at(Z: np.ndarray, g: int, n: int) -> int:
+    """Zero point of K-group g, column n: the low nibble of byte Z[g][n], two's
+    complement."""
+    z = np.ascontiguousarray(Z, dtype=np.int8)
+    return int(lib().oracle_zero_at(z.ctypes.data, z.shape[1], g, n))
 
 
 def unpack_int4(packed: np.ndarray) -> np.ndarray:
@@ -168,6 +178,10 @@ def _desc(p, keep):
             np.uint32 if p.v_type == F32 else np.uint16)
         keep.append(V)
         g.v_type, g.V, g.ldv, g.gb = p.v_type, V.ctypes.data, p.N, p.gb
+    if getattr(p, "Z", None) is not None:
+        Z = _arr(p.Z, np.int8)
+        keep.append(Z)
+        g.Z, g.ldz = Z.ctypes.data, p.N
     g.alpha, g.beta = float(p.alpha), float(p.beta)
     g.epilogue = int(getattr(p, "epilogue", 0) or 0)
     if g.epilogue & 1:

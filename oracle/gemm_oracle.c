@@ -14,6 +14,8 @@
  *    DeepGEMM kernel-set blog, section 1.1.
  *  - U/V are group-wise scales that advance at K-group boundaries:
  *    "InternLM Lmdeploy Gemm MainloopSm80V2", section Description (GroupIter).
+ *    Asymmetric int4 weights add a zero point z per (K-group, column) that
+ *    advances the same way: b-hat = RN_A((q - z) * v).
  *  - FP8 (E4M3 / E5M2) operands, among the quantised inputs the DeepGEMM
  *    kernel-set blog targets (sections 1.2 and 6.3): decoded exactly like the
  *    16-bit ones; every product of two of them is exact in double.
@@ -180,6 +182,8 @@ typedef struct {
     double alpha, beta;
     int epilogue;               /* bit 0: + bias[j]; bit 1: ReLU; bit 2: GELU     */
     int bias_type; const void* bias;                    /* N values (bit 0)     */
+    const void* Z; int64_t ldz; /* int4 B with V: zero points [K/gb][N], one per
+                                   byte (low nibble, two's complement), or 0   */
 } oracle_gemm_t;
 
 static uint32_t load_bits(int type, const void* p, int64_t idx)
@@ -210,8 +214,17 @@ int oracle_int4_at(const uint8_t* B, int64_t ldb, int64_t n, int64_t k)
     return nib >= 8 ? nib - 16 : nib;
 }
 
+/* Zero point of K-group g, column j: the two's-complement value of the low
+ * nibble of byte [g][j] (a 4-bit zero point stored one per byte). */
+int oracle_zero_at(const uint8_t* Z, int64_t ldz, int64_t g, int64_t j)
+{
+    int nib = Z[g * ldz + j] & 0xF;
+    return nib >= 8 ? nib - 16 : nib;
+}
+
 /* b-hat[k][j]: B's stored value (B is stored N x K), or the dequantised value.
- * 16-bit B with V: RN_B(b * v).  int4 B: RN_A(q * v), or q without V. */
+ * 16-bit B with V: RN_B(b * v).  int4 B: RN_A((q - z) * v), with z = 0 unless
+ * zero points are given (asymmetric quantisation), or q without V. */
 static double b_hat(const oracle_gemm_t* P, int64_t k, int64_t j)
 {
     double v = 1.0;
@@ -221,6 +234,8 @@ static double b_hat(const oracle_gemm_t* P, int64_t k, int64_t j)
         int q = oracle_int4_at((const uint8_t*)P->B, P->ldb, j, k);
         if (!P->V)
             return (double)q;
+        if (P->Z)
+            q -= oracle_zero_at((const uint8_t*)P->Z, P->ldz, k / P->gb, j);
         return oracle_decode(P->a_type, oracle_encode_rn(P->a_type, (double)q * v));
     }
     double b = oracle_decode(P->b_type, load_bits(P->b_type, P->B, j * P->ldb + k));
@@ -236,6 +251,8 @@ static int check(const oracle_gemm_t* P)
     if (P->U && (P->ga <= 0 || P->K % P->ga))
         return 1;
     if (P->V && (P->gb <= 0 || P->K % P->gb))
+        return 1;
+    if (P->Z && (!P->V || P->b_type != OR_S4))
         return 1;
     if (P->beta != 0.0 && !P->C)
         return 1;

@@ -83,6 +83,7 @@ class Problem:
     V: np.ndarray | None = None      # [K/gb][N]
     v_type: int | None = None
     gb: int = 0
+    Z: np.ndarray | None = None      # int4 B with V: [K/gb][N] int8 zero points in [-8, 7]
     U: np.ndarray | None = None      # [K/ga][M]
     u_type: int | None = None
     ga: int = 0
@@ -145,14 +146,18 @@ def config2_fp8(seed=1002, M=4096, N=4096, K=4096, a_type=E4M3) -> Problem:
 
 
 def w4a16(M, N, K, *, seed, group=128, a_type=BF16, d_type=BF16, vlo=0.005, vhi=0.02,
-          name="") -> Problem:
-    """Int4 weights with fp16 per-(group, column) scales; A ~ N(0,1)."""
+          zero=False, name="") -> Problem:
+    """Int4 weights with fp16 per-(group, column) scales; A ~ N(0,1).  zero=True
+    adds asymmetric zero points, uniform integers in [-8, 7] per (group, column)."""
     g = _rng(seed)
     a = g.standard_normal(size=(M, K), dtype=np.float32)
     q = g.integers(-8, 8, size=(N, K), dtype=np.int64)
     v = g.uniform(vlo, vhi, size=(K // group, N)).astype(np.float32)
-    return Problem(M, N, K, a_type, S4, d_type, _round_bits(a, a_type), pack_int4(q),
-                   V=_round_bits(v, F16), v_type=F16, gb=group, name=name or f"W4A16 {M}x{N}x{K}")
+    p = Problem(M, N, K, a_type, S4, d_type, _round_bits(a, a_type), pack_int4(q),
+                V=_round_bits(v, F16), v_type=F16, gb=group, name=name or f"W4A16 {M}x{N}x{K}")
+    if zero:
+        p.Z = g.integers(-8, 8, size=(K // group, N), dtype=np.int64).astype(np.int8)
+    return p
 
 
 def config4(seed=1004, M=128, N=11008, K=4096) -> Problem:

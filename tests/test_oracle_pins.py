@@ -498,3 +498,49 @@ def test_fp8_identity_b_closed_form(dtype, one):
     p.B = np.where(np.eye(K, dtype=bool), np.uint8(one), np.uint8(0)).astype(np.uint8)
     ref, _ = oracle.gemm(p)
     assert np.array_equal(ref, 1.5 * lib_decode_fp8(dtype, p.A) + 0.5 * lib_decode(BF16, p.C))
+
+
+# ---- asymmetric int4: a zero point per (K-group, column) ------------------------
+
+def test_zero_point_byte_rule():
+    # a 4-bit zero point stored one per byte: the low nibble, two's complement
+    table = {0x00: 0, 0x07: 7, 0x08: -8, 0x0F: -1, 0x09: -7, 0xF3: 3, 0x80: 0, 0x7C: -4}
+    Z = np.array([list(table)], dtype=np.uint8).view(np.int8)
+    assert [oracle.zero_at(Z, 0, n) for n in range(len(table))] == list(table.values())
+
+
+def test_zero_point_unit_scale_exposes_q_minus_z():
+    M, N, K, g = 16, 12, 256, 64
+    p = synth.w4a16(M, N, K, seed=33, group=g, zero=True)
+    p.V = np.full_like(p.V, 0x3C00)           # fp16 1.0
+    ks = np.random.default_rng(4).integers(0, K, M)
+    p.A = _one_hot_a(M, K, ks, BF16)
+    ref, _ = oracle.gemm(p)
+    q = oracle.unpack_int4(p.B)                # N x K
+    z = p.Z.astype(np.int64)[np.arange(K) // g, :].T   # N x K
+    assert np.array_equal(ref, (q - z)[:, ks].T.astype(np.float64))
+
+
+@pytest.mark.parametrize("a_type", [BF16, F16])
+def test_zero_point_dequant_rounding_matches_torch(a_type):
+    M, N, K = 24, 40, 512
+    p = synth.w4a16(M, N, K, seed=34, group=128, zero=True, a_type=a_type)
+    ks = np.random.default_rng(5).integers(0, K, M)
+    p.A = _one_hot_a(M, K, ks, a_type)
+    ref, _ = oracle.gemm(p)
+    q = oracle.unpack_int4(p.B).astype(np.float32)                          # N x K
+    z = p.Z.astype(np.float32)[np.arange(K) // 128, :].T
+    v = lib_decode(F16, p.V).astype(np.float32)[np.arange(K) // 128, :].T  # N x K
+    prod = (q - z) * v                                                      # exact in fp32
+    tdt = torch.bfloat16 if a_type == BF16 else torch.float16
+    bhat = torch.from_numpy(prod).to(tdt).to(torch.float64).numpy()
+    assert np.array_equal(ref, bhat[:, ks].T)
+
+
+def test_zero_points_of_zero_are_symmetric():
+    p = synth.w4a16(9, 20, 256, seed=35, group=128, zero=True)
+    p.Z = np.zeros_like(p.Z)
+    r1, b1 = oracle.gemm(p)
+    p.Z = None
+    r2, b2 = oracle.gemm(p)
+    assert np.array_equal(r1, r2) and np.array_equal(b1, b2)
