@@ -148,6 +148,18 @@ typedef struct {
     int32_t out_zero_point;/* GEMM_S8 D: the zero point zp                           */
     const float* out_scale;/* GEMM_S8 D: M fp32 scales on the device, one per row of D
                               (per token); ignored for other D types                  */
+    /* Asymmetric int4 B (zero points advance at K-group boundaries with V, as
+     * the scale operands of "InternLM Lmdeploy Gemm MainloopSm80V2", section
+     * Description, do): B-hat[k][j] = RN_A((q[k][j] - z[k/gb][j]) * V[k/gb][j]).
+     * z is a 4-bit two's-complement zero point in [-8, 7] stored one per byte
+     * (the byte's low nibble; its high nibble is ignored), in a (K/gb) x N
+     * row-major byte matrix on the device.  NULL means symmetric (z = 0).
+     * Needs an int4 B with V; b_zero 16-byte aligned, b_zero_ld (bytes between
+     * rows, >= N) a multiple of 16; grouped problems give one matrix per expert,
+     * b_zero_batch_stride bytes apart (a multiple of 16).                     */
+    const void* b_zero;
+    int64_t b_zero_ld;
+    int64_t b_zero_batch_stride;
 } gemm_op_t;
 
 /*
@@ -243,7 +255,11 @@ int gemm_run_noalloc(gemm_handle_t h, const gemm_op_t* op, float alpha,
  *   col-major, batch_stride apart;  C, D : (sum m_e) x N row-major.
  *   expert_offsets_dev: DEVICE int32[num_experts + 1], prefix sums starting at
  *   0 and ending at Adesc->rows; read on the device only (no host sync).
- *   Experts with zero rows are allowed.  U/V are not served here (pass NULL).
+ *   Experts with zero rows are allowed.
+ *   U (optional): (K/ga) x (sum m_e) row-major, one scale per token row and
+ *   K-group, num = 1.  V (optional, and the zero points of gemm_op_t):
+ *   num = num_experts matrices (K/gb) x N, batch_stride apart, one per expert
+ *   (a W4A16 mixture of experts with an int4 B).
  */
 int gemm_run_grouped(gemm_handle_t h, const gemm_op_t* op, float alpha,
                      const void* A, const gemm_layout_t* Adesc,

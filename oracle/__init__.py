@@ -239,11 +239,19 @@ class _Slice:
 
     def __init__(self, gp, e, rows=None):
         lo, hi = int(gp.offsets[e]), int(gp.offsets[e + 1])
-        self.M = hi - lo if rows is None else len(rows)
+        idx = np.arange(lo, hi) if rows is None else lo + np.asarray(rows, dtype=np.int64)
+        self.M = len(idx)
         self.N, self.K = gp.N, gp.K
-        self.a_type = self.b_type = gp.a_type
-        self.A = gp.A[lo:hi] if rows is None else gp.A[lo + np.asarray(rows)]
+        self.a_type = gp.a_type
+        self.b_type = gp.b_type if getattr(gp, "b_type", None) is not None else gp.a_type
+        self.A = gp.A[idx]
         self.B = gp.B[e]
+        # per-expert V (and zero points); U holds one scale per token row
+        self.V = gp.V[e] if getattr(gp, "V", None) is not None else None
+        self.v_type, self.gb = getattr(gp, "v_type", None), getattr(gp, "gb", 0)
+        self.Z = gp.Z[e] if getattr(gp, "Z", None) is not None else None
+        self.U = np.ascontiguousarray(gp.U[:, idx]) if getattr(gp, "U", None) is not None else None
+        self.u_type, self.ga = getattr(gp, "u_type", None), getattr(gp, "ga", 0)
         self.alpha, self.beta = gp.alpha, gp.beta
         self.C = None
         self.c_type = None
@@ -253,8 +261,9 @@ class _Slice:
 
 def grouped(gp):
     """Grouped GEMM as the loop of per-expert GEMMs it is defined to be:
-    rows offsets[e]..offsets[e+1] of A times expert e's B.  Returns (ref, bound)
-    of shape [sum m_e, N]."""
+    rows offsets[e]..offsets[e+1] of A times expert e's B (dequantised with
+    expert e's V and zero points, A's rows scaled by their U columns).
+    Returns (ref, bound) of shape [sum m_e, N]."""
     T = int(gp.offsets[-1])
     ref = np.empty((T, gp.N), dtype=np.float64)
     bound = np.empty((T, gp.N), dtype=np.float64)

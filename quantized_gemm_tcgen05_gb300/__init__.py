@@ -64,7 +64,8 @@ class gemm_op_t(ctypes.Structure):
     _fields_ = [("dispatch", ctypes.c_int32), ("epilogue", ctypes.c_int32), ("quant_a_group", ctypes.c_int32),
                 ("quant_b_group", ctypes.c_int32), ("splitk", ctypes.c_int32), ("streamk", ctypes.c_int32),
                 ("bias", ctypes.c_void_p), ("bias_type", ctypes.c_int32), ("out_zero_point", ctypes.c_int32),
-                ("out_scale", ctypes.c_void_p)]
+                ("out_scale", ctypes.c_void_p), ("b_zero", ctypes.c_void_p), ("b_zero_ld", ctypes.c_int64),
+                ("b_zero_batch_stride", ctypes.c_int64)]
 
 
 class gemm_workspace_t(ctypes.Structure):

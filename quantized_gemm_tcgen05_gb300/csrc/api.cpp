@@ -246,15 +246,15 @@ int make_map_kchunk4(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t ty
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-// Tensor map over packed int4 rows: [rows][K/2 bytes], box 32 bytes x rows,
-// no swizzle (the dequantising warps rewrite the tile into the swizzled
-// layout the tensor core reads).
+// Tensor map over packed int4 rows: [batches][rows][K/2 bytes], box 32 bytes
+// x rows, no swizzle (the dequantising warps rewrite the tile into the
+// swizzled layout the tensor core reads).
 int make_map_s4(gemm_handle* h, CUtensorMap* m, const void* ptr, int64_t K, int64_t rows, int64_t ld_nibbles,
-                int32_t box_rows) {
-    cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)(ld_nibbles / 2)};
-    cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
-    CUresult r = encode_cached(h, m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, strides, box,
+                int32_t box_rows, int32_t batches = 1, int64_t bstride_nibbles = 0) {
+    cuuint64_t dims[3] = {(cuuint64_t)(K / 2), (cuuint64_t)rows, (cuuint64_t)batches};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld_nibbles / 2), (cuuint64_t)(bstride_nibbles / 2)};
+    cuuint32_t box[3] = {32, (cuuint32_t)box_rows, 1};
+    CUresult r = encode_cached(h, m, CU_TENSOR_MAP_DATA_TYPE_UINT8, batches > 1 ? 3 : 2, ptr, dims, strides, box,
                                CU_TENSOR_MAP_SWIZZLE_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -277,15 +277,28 @@ int make_map_cd(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t type, i
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-// Tensor map over a [groups][cols] row-major scale matrix (U or V): each
-// K-step copies box_rows group rows x box_cols columns into its stage.
+// Tensor map over a [batches][groups][cols] row-major scale matrix (U or V;
+// one per expert for grouped problems): each K-step copies box_rows group
+// rows x box_cols columns into its stage.
 int make_map_scale(gemm_handle* h, CUtensorMap* m, const void* ptr, int32_t type, int64_t groups, int64_t cols,
-                   int64_t ld, int32_t box_cols, int32_t box_rows) {
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)groups};
-    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+                   int64_t ld, int32_t box_cols, int32_t box_rows, int32_t batches = 1, int64_t bstride = 0) {
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)groups, (cuuint64_t)batches};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld * 2), (cuuint64_t)(bstride * 2)};
+    cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
     CUtensorMapDataType dt = type == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUresult r = encode_cached(h, m, dt, 2, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    CUresult r = encode_cached(h, m, dt, batches > 1 ? 3 : 2, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// Tensor map over the [batches][groups][cols] byte matrix of int4 zero points,
+// boxed like the scale rows.
+int make_map_zero(gemm_handle* h, CUtensorMap* m, const void* ptr, int64_t groups, int64_t cols, int64_t ld,
+                  int32_t box_cols, int32_t box_rows, int32_t batches, int64_t bstride) {
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)groups, (cuuint64_t)batches};
+    cuuint64_t strides[2] = {(cuuint64_t)ld, (cuuint64_t)bstride};
+    cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
+    CUresult r = encode_cached(h, m, CU_TENSOR_MAP_DATA_TYPE_UINT8, batches > 1 ? 3 : 2, ptr, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -335,6 +348,8 @@ int launch_gemv_choice(gemm_handle* h, const Problem& p, cudaStream_t st) {
     g.A = p.A;
     g.B = p.B;
     g.V = p.V;
+    g.Z = p.Z;
+    g.ldz = p.ldz;
     g.C = p.beta != 0.0f ? p.C : nullptr;
     g.D = p.D;
     g.lda = p.lda;
@@ -389,8 +404,8 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
     e.C = p.beta != 0.0f ? p.C : nullptr;
     e.ldd = p.ldd;
     e.ldc = p.ldc;
-    e.d_bstride = p.family == FAM_GROUPED ? 0 : p.d_bs;
-    e.c_bstride = p.family == FAM_GROUPED ? 0 : p.c_bs;
+    e.d_bstride = is_grouped(p) ? 0 : p.d_bs;
+    e.c_bstride = is_grouped(p) ? 0 : p.c_bs;
     e.M = p.M;
     e.N = p.N;
     e.alpha = p.alpha;
@@ -418,9 +433,18 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
     CUtensorMap& tx = maps.x;
     CUtensorMap& ty = maps.y;
     int rc;
-    const bool dq = p.family == FAM_DQ;
+    const bool dq = is_dq(p);
     const bool s4 = p.b_type == GEMM_S4;
-    if (p.family == FAM_GROUPED && c.pair && pair_kchunks(p) > 1) {
+    if (p.family == FAM_GROUPED_DQ) {
+        // experts' int4 or 16-bit B, one slice per expert (the Y operand's
+        // third coordinate); A (the token rows) is one 2-D operand
+        rc = make_map(h, &tx, p.A, p.a_type, p.K, p.M, p.lda, 1, 0, 128);
+        if (rc == GEMM_OK)
+            rc = s4 ? make_map_s4(h, &ty, p.B, p.K, p.N, p.ldb, c.bn, p.num_experts, p.b_bs)
+                    : make_map(h, &ty, p.B, p.b_type, p.K, p.N, p.ldb, p.num_experts, p.b_bs, c.bn);
+        kp.x3d = 0;
+        kp.y3d = p.num_experts > 1;
+    } else if (p.family == FAM_GROUPED && c.pair && pair_kchunks(p) > 1) {
         // 256-row expert blocks on CTA pairs: each CTA its 128 token rows and
         // half of the expert's Y tile, several K-steps per copy
         const int ks = pair_kchunks(p);
@@ -475,7 +499,7 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
         };
         const char* et = getenv("GEMM_EPI_TMA");
         const bool allowed = !(et && et[0] == '0');
-        e.tma = allowed && !c.swap && p.family != FAM_GROUPED && c.bn >= 32 && p.d_type != GEMM_S8 &&
+        e.tma = allowed && !c.swap && !is_grouped(p) && c.bn >= 32 && p.d_type != GEMM_S8 &&
                 ok16(p.D, p.ldd, p.d_bs) &&
                 (e.C == nullptr || ok16(p.C, p.ldc, p.c_bs)) && !(c.pair && es == 4);
         if (e.tma) {
@@ -494,6 +518,7 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
         auto xform = [](const void* scale, int32_t type, int32_t group, int32_t int4) {
             OperandXform o;
             o.has_scale = scale != nullptr;
+            o.has_zero = 0;
             o.scale_type = type;
             o.group = scale ? group : 64;
             o.sc_rows = scale ? (group >= 64 ? 1 : 64 / group) : 0;
@@ -502,7 +527,8 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
             return o;
         };
         const OperandXform a_side = xform(p.U, p.u_type, p.ga, 0);
-        const OperandXform b_side = xform(p.V, p.v_type, p.gb, s4 ? 1 : 0);
+        OperandXform b_side = xform(p.V, p.v_type, p.gb, s4 ? 1 : 0);
+        b_side.has_zero = p.Z != nullptr;
         d.x = c.swap ? b_side : a_side;
         d.y = c.swap ? a_side : b_side;
         // scale rows: X side tiles are 128 rows, Y side tiles are BN rows
@@ -510,14 +536,23 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
         const void* ys_ptr = c.swap ? p.U : p.V;
         if (xs_ptr) {
             const bool v = c.swap;
+            // 136 columns: the copy starts at the 8-aligned column below the
+            // tile's first row (token blocks of grouped problems start anywhere)
             rc = make_map_scale(h, &maps.xs, xs_ptr, v ? p.v_type : p.u_type, p.K / (v ? p.gb : p.ga), v ? p.N : p.M,
-                                v ? p.ldv : p.ldu, 128, d.x.sc_rows);
+                                v ? p.ldv : p.ldu, 136, d.x.sc_rows);
             if (rc != GEMM_OK) return rc;
         }
         if (ys_ptr) {
             const bool v = !c.swap;
+            const int32_t nb = v && kp.y3d ? p.num_experts : 1;  // grouped: V per expert
             rc = make_map_scale(h, &maps.ys, ys_ptr, v ? p.v_type : p.u_type, p.K / (v ? p.gb : p.ga), v ? p.N : p.M,
-                                v ? p.ldv : p.ldu, c.bn, d.y.sc_rows);
+                                v ? p.ldv : p.ldu, c.bn, d.y.sc_rows, nb, v ? p.v_bs : 0);
+            if (rc != GEMM_OK) return rc;
+        }
+        if (p.Z) {  // zero points of the int4 B, on whichever side B is
+            const int32_t nb = !c.swap && kp.y3d ? p.num_experts : 1;
+            rc = make_map_zero(h, &maps.z, p.Z, p.K / p.gb, p.N, p.ldz, c.swap ? 128 : c.bn,
+                               c.swap ? d.x.sc_rows : d.y.sc_rows, nb, p.z_bs);
             if (rc != GEMM_OK) return rc;
         }
         kp.stages = umma_dq_max_stages(c.bn);
@@ -609,12 +644,12 @@ bool forced_kernel(const Problem& p, Choice* out) {
     }
     if (!(c.bn == 16 || c.bn == 32 || c.bn == 64 || c.bn == 128 || c.bn == 192 || c.bn == 224 || c.bn == 256))
         return false;
-    if (p.family == FAM_DQ && (c.bn == 192 || c.bn == 224)) return false;
-    if (c.swap && (p.family == FAM_GROUPED || p.batches != 1)) return false;
+    if (is_dq(p) && (c.bn == 192 || c.bn == 224)) return false;
+    if (c.swap && (is_grouped(p) || p.batches != 1)) return false;
     if (c.pair && ((p.family != FAM_DENSE && p.family != FAM_GROUPED) || c.swap || c.sched == SCHED_SPLITK ||
                    !(c.bn == 128 || c.bn == 224 || c.bn == 256)))
         return false;
-    if (p.family == FAM_GROUPED) c.sched = SCHED_DP;
+    if (is_grouped(p)) c.sched = SCHED_DP;
     *out = c;
     return true;
 }
@@ -626,7 +661,7 @@ bool forced_kernel(const Problem& p, Choice* out) {
 // schedule does not fit.
 template <typename Fits>
 bool settle_schedule(const Problem& p, Choice* c, bool forced, const Fits& fits) {
-    if (p.family == FAM_GROUPED) c->sched = SCHED_DP;
+    if (is_grouped(p)) c->sched = SCHED_DP;
     if (!fits(*c) && c->sched != SCHED_DP && !c->swap && c->bn > 128) {
         Choice narrower = *c;  // half-width tiles halve the partial-tile footprint
         narrower.bn = 128;
@@ -832,18 +867,33 @@ int build_problem(gemm_handle* h, const gemm_op_t* op, float alpha, const void* 
         if (p.gb < 8 || p.K % p.gb || (p.gb % 64 && 64 % p.gb)) return GEMM_ERR_INVALID_ARG;
         if (!is16(Vdesc->type)) return GEMM_ERR_UNSUPPORTED;
         if ((rc = check_layout(Vdesc, GEMM_ROW_MAJOR, p.K / p.gb, p.N))) return rc;
-        if (Vdesc->num != 1) return GEMM_ERR_UNSUPPORTED;
+        // grouped problems: one V per expert (as many as B has matrices)
+        if (Vdesc->num != (grouped ? Bdesc->num : 1)) return grouped ? GEMM_ERR_INVALID_ARG : GEMM_ERR_UNSUPPORTED;
         if (!aligned16(V) || (Vdesc->ld * 2) % 16) return GEMM_ERR_INVALID_ARG;  // copied by TMA
+        if (Vdesc->num > 1 && (Vdesc->batch_stride < (p.K / p.gb) * Vdesc->ld || (Vdesc->batch_stride * 2) % 16))
+            return GEMM_ERR_INVALID_ARG;
         p.V = V;
         p.ldv = Vdesc->ld;
+        p.v_bs = Vdesc->num > 1 ? Vdesc->batch_stride : 0;
         p.v_type = Vdesc->type;
+    }
+    if (op->b_zero) {
+        // zero points of an int4 B with V: (K/gb) x N bytes per expert, copied by TMA
+        if (!p.V || p.b_type != GEMM_S4) return GEMM_ERR_INVALID_ARG;
+        if (!aligned16(op->b_zero) || op->b_zero_ld < p.N || op->b_zero_ld % 16) return GEMM_ERR_INVALID_ARG;
+        const int64_t nz = grouped ? Bdesc->num : 1;
+        if (nz > 1 && (op->b_zero_batch_stride < (p.K / p.gb) * op->b_zero_ld || op->b_zero_batch_stride % 16))
+            return GEMM_ERR_INVALID_ARG;
+        if (p.N > 0 && p.K > 0 && !device_pointer(h, op->b_zero)) return GEMM_ERR_INVALID_ARG;
+        p.Z = op->b_zero;
+        p.ldz = op->b_zero_ld;
+        p.z_bs = nz > 1 ? op->b_zero_batch_stride : 0;
     }
     p.family = (p.U || p.V || p.b_type == GEMM_S4) ? FAM_DQ : FAM_DENSE;
     if (is_f8(p.a_type) && p.family != FAM_DENSE) return GEMM_ERR_UNSUPPORTED;  // no U/V on 8-bit operands
     if (grouped) {
-        if (p.U || p.V || p.b_type == GEMM_S4) return GEMM_ERR_UNSUPPORTED;
         if (Adesc->num != 1 || Ddesc->num != 1) return GEMM_ERR_INVALID_ARG;
-        p.family = FAM_GROUPED;
+        p.family = p.family == FAM_DQ ? FAM_GROUPED_DQ : FAM_GROUPED;
         p.batches = 1;
     } else {
         if (Bdesc->num != p.batches || Ddesc->num != p.batches) return GEMM_ERR_INVALID_ARG;
@@ -864,7 +914,7 @@ int build_problem(gemm_handle* h, const gemm_op_t* op, float alpha, const void* 
         const int64_t es = in_bytes(p.a_type);
         if ((p.lda * es) % 16 || (p.a_bs * es) % 16) return GEMM_ERR_INVALID_ARG;
         if (p.b_type == GEMM_S4) {
-            if (p.K % 2 || p.ldb % 32) return GEMM_ERR_INVALID_ARG;
+            if (p.K % 2 || p.ldb % 32 || p.b_bs % 32) return GEMM_ERR_INVALID_ARG;
         } else if ((p.ldb * es) % 16 || (p.b_bs * es) % 16) {
             return GEMM_ERR_INVALID_ARG;
         }
@@ -1043,8 +1093,7 @@ int gemm_heuristic_choice(int64_t m, int64_t n, int64_t k, int32_t a_type, int32
     }
     p.family = (p.U || p.V || b_type == GEMM_S4) ? FAM_DQ : FAM_DENSE;
     if (num_experts > 0) {
-        if (p.family != FAM_DENSE) return GEMM_ERR_INVALID_ARG;
-        p.family = FAM_GROUPED;
+        p.family = p.family == FAM_DQ ? FAM_GROUPED_DQ : FAM_GROUPED;
         p.num_experts = num_experts;
     }
     Choice c = heuristic(p, sm_count, partials_size);

@@ -52,7 +52,7 @@ SchedParams make_sched(const Problem& p, const Choice& c, int sm_count) {
     memset(&s, 0, sizeof s);
     s.k_iters = (int32_t)ceil_div(p.K, kstep_of(p));
     s.batches = p.batches;
-    if (p.family == FAM_GROUPED) {
+    if (is_grouped(p)) {
         // upper bound on padded M-blocks: sum_e ceil(m_e / bm) <= T / bm + E
         // (bm = 256 rows on CTA pairs)
         s.tiles_x = (int32_t)(p.M / (c.pair ? 256 : 128) + p.num_experts);
@@ -155,7 +155,7 @@ std::vector<Choice> candidates(const Problem& p, int sm_count) {
         c.swap = swap;
         c.sched = SCHED_DP;
         out.push_back(c);
-        if (p.family == FAM_GROUPED) return;
+        if (is_grouped(p)) return;
         SchedParams s = make_sched(p, c, sm_count);
         const int64_t T = total_tiles(s);
         if (k_iters >= 2 && T < 4 * (int64_t)sm_count) {
@@ -173,7 +173,7 @@ std::vector<Choice> candidates(const Problem& p, int sm_count) {
             }
         }
     };
-    if (p.family == FAM_DQ) {
+    if (is_dq(p)) {
         for (int32_t bn : {64, 128, 256})
             if (bn == 64 || p.N > bn / 2) add_scheds(bn, 0);
         if (swap_allowed(p)) add_scheds(swap_bn(p.M), 1);
@@ -212,7 +212,7 @@ Choice heuristic(const Problem& p, int sm_count, size_t partials_bytes, bool all
     if (swap_allowed(p) && p.M <= 64) {
         c.swap = 1;
         c.bn = swap_bn(p.M);
-    } else if (p.family == FAM_DQ || p.N <= 128) {
+    } else if (is_dq(p) || p.N <= 128) {
         c.bn = 128;
     } else if (p.family == FAM_GROUPED) {
         // 256-row expert blocks on CTA pairs once they fill a wave of clusters
@@ -271,7 +271,7 @@ Choice heuristic(const Problem& p, int sm_count, size_t partials_bytes, bool all
         }
     }
     c.sched = SCHED_DP;
-    if (p.family == FAM_GROUPED) return c;
+    if (is_grouped(p)) return c;
     SchedParams s = make_sched(p, c, sm_count);
     const int64_t T = total_tiles(s);
     const int64_t k_iters = s.k_iters;
@@ -291,7 +291,10 @@ std::string choice_name(const Problem& p, const Choice& c) {
     char buf[96];
     const char* fam = p.family == FAM_DQ
                           ? "umma_dq"
-                          : (p.family == FAM_GROUPED ? (c.pair ? "umma2_grouped" : "umma_grouped") : (c.pair ? "umma2" : "umma"));
+                          : (p.family == FAM_GROUPED_DQ
+                                 ? "umma_dq_grouped"
+                                 : (p.family == FAM_GROUPED ? (c.pair ? "umma2_grouped" : "umma_grouped")
+                                                            : (c.pair ? "umma2" : "umma")));
     const char* sk = c.sched == SCHED_DP ? "dp" : (c.sched == SCHED_STREAMK ? "streamk" : "splitk");
     if (c.sched == SCHED_SPLITK)
         snprintf(buf, sizeof buf, "%s_bn%d%s/%s%d", fam, c.bn, c.swap ? "_swap" : "", sk, c.splits);
@@ -346,7 +349,7 @@ static bool valid_choice(const Key& k, const Choice& c) {
         return false;
     if (c.pair && (c.swap || c.sched == SCHED_SPLITK || (k.family != FAM_DENSE && k.family != FAM_GROUPED))) return false;
     if (c.pair && c.bn != 128 && c.bn != 224 && c.bn != 256) return false;
-    if (k.family < FAM_DENSE || k.family > FAM_GROUPED) return false;
+    if (k.family < FAM_DENSE || k.family > FAM_GROUPED_DQ) return false;
     if (k.N < 0 || k.K < 0 || k.m_bucket < 1 || k.batches < 1) return false;
     return true;
 }

@@ -13,7 +13,9 @@
 
 namespace qg {
 
-enum Family : int32_t { FAM_DENSE = 0, FAM_DQ = 1, FAM_GROUPED = 2 };
+// Problem families: dense; with operand transforms (U/V scales, int4 B);
+// grouped (MoE); grouped with operand transforms (e.g. W4A16 experts).
+enum Family : int32_t { FAM_DENSE = 0, FAM_DQ = 1, FAM_GROUPED = 2, FAM_GROUPED_DQ = 3 };
 
 // A validated, normalised problem.  Operand X feeds the UMMA M side (128
 // rows per tile), operand Y the N side; which of A / B each one is depends on
@@ -27,7 +29,8 @@ struct Problem {
     const void* A; int64_t lda, a_bs;
     const void* B; int64_t ldb, b_bs;   // stored N x K (K contiguous); S4: ld in nibbles
     const void* U; int64_t ldu; int32_t u_type, ga;
-    const void* V; int64_t ldv; int32_t v_type, gb;
+    const void* V; int64_t ldv, v_bs; int32_t v_type, gb;   // v_bs: grouped, elements between experts
+    const void* Z; int64_t ldz, z_bs;                         // int4 zero points (bytes), or null
     const void* C; int64_t ldc, c_bs;
     void* D; int64_t ldd, d_bs;
     float alpha, beta;
@@ -67,6 +70,9 @@ Key make_key(const Problem& p);
 SchedParams make_sched(const Problem& p, const Choice& c, int sm_count);
 size_t partials_bytes_needed(const SchedParams& s, int bn, int pair);
 size_t counters_bytes_needed(const SchedParams& s, int pair);
+
+inline bool is_grouped(const Problem& p) { return p.family == FAM_GROUPED || p.family == FAM_GROUPED_DQ; }
+inline bool is_dq(const Problem& p) { return p.family == FAM_DQ || p.family == FAM_GROUPED_DQ; }
 
 // Elements per K-step (one 128-byte swizzle row) of the problem's operands.
 inline int32_t kstep_of(const Problem& p) { return p.kstep > 0 ? p.kstep : BK_HOST; }

@@ -9,8 +9,9 @@
 // at most one wave of resident CTAs and walks the row groups with a stride.
 //
 // Per element: b^ = b (16-bit B, no scale), RN_A(b * v) (16-bit B with V) or
-// RN_A(q * v) (int4 B, unscaled: q), each product exact in fp32 and rounded
-// once to A's type; then acc += a * b^ in fp32 (exact product, fp32 sum).
+// RN_A((q - z) * v) (int4 B, z = 0 without zero points; unscaled: q), each
+// product exact in fp32 and rounded once to A's type; then acc += a * b^ in
+// fp32 (exact product, fp32 sum).
 #include <atomic>
 
 #include "gemv.h"
@@ -58,23 +59,36 @@ __device__ __forceinline__ void round2(float& a, float& b) {
     }
 }
 
+// Group of the 8-value block i8 along K: i8 / (gb / 8), by a multiply exact
+// for i8 < 2^24.
+__device__ __forceinline__ int64_t group_of(uint64_t gmagic, int64_t i8) {
+    return (int64_t)(((uint64_t)i8 * gmagic) >> 40);
+}
+
 __device__ __forceinline__ float scale_at(const GemvParams& p, uint64_t gmagic, int64_t n, int64_t i8) {
-    // group of the 8-value block i8: i8 / (gb / 8), by a multiply exact for i8 < 2^24
-    const int64_t g = (int64_t)(((uint64_t)i8 * gmagic) >> 40);
-    const uint16_t bits = reinterpret_cast<const uint16_t*>(p.V)[g * p.ldv + n];
+    const uint16_t bits = reinterpret_cast<const uint16_t*>(p.V)[group_of(gmagic, i8) * p.ldv + n];
     return p.v_bf16 ? __uint_as_float((uint32_t)bits << 16) : __half2float(__ushort_as_half(bits));
 }
 
-// A group scale prepared for dequant8: for bf16 results the split pair
-// (vhi2, vlo2) of the packed path, else the fp32 value.
+// Zero point of column n for block i8: the low nibble of its byte, two's
+// complement; 0 without zero points.
+__device__ __forceinline__ int zero_at(const GemvParams& p, uint64_t gmagic, int64_t n, int64_t i8) {
+    if (!p.Z) return 0;
+    const uint8_t b = reinterpret_cast<const uint8_t*>(p.Z)[group_of(gmagic, i8) * p.ldz + n];
+    return (int)((uint32_t)b << 28) >> 28;
+}
+
+// A group scale and zero point prepared for dequant8: for bf16 results the
+// split pair (vhi2, vlo2) and the offset pair of the packed path, else the
+// fp32 value and the magic-number bias 2^23 + 8 + z.
 struct Scale {
-    uint32_t vhi2, vlo2;
-    float v;
+    uint32_t vhi2, vlo2, off2;
+    float v, zoff;
 };
 
 template <bool BF16>
-__device__ __forceinline__ Scale prep_scale(float v, bool scaled) {
-    Scale s{0x3F803F80u, 0u, scaled ? v : 1.0f};  // unscaled: v = 1
+__device__ __forceinline__ Scale prep_scale(float v, bool scaled, int z = 0) {
+    Scale s{0x3F803F80u, 0u, int4_off2(z), scaled ? v : 1.0f, 8388616.0f + (float)z};  // unscaled: v = 1
     if (BF16 && scaled) split_scale_bf16(v, s.vhi2, s.vlo2);
     return s;
 }
@@ -88,20 +102,21 @@ __device__ __forceinline__ void dequant8(uint32_t w, const Scale& sc, float* f) 
         const uint32_t w4 = w >> 4;
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-            const uint32_t pr =
-                int4_pair_bf16(__byte_perm(w, w4, (uint32_t)t * 0x11u | (uint32_t)(4 + t) * 0x1100u), vhi2, vlo2);
+            const uint32_t pr = int4_pair_bf16(__byte_perm(w, w4, (uint32_t)t * 0x11u | (uint32_t)(4 + t) * 0x1100u),
+                                               vhi2, vlo2, sc.off2);
             f[2 * t] = lo_bf16(pr);
             f[2 * t + 1] = hi_bf16(pr);
         }
     } else {
-        // biased nibble u = q + 8 becomes the float 2^23 + u, so q = f - (2^23 + 8)
+        // biased nibble u = q + 8 becomes the float 2^23 + u, so
+        // q - z = f - (2^23 + 8 + z), exactly
         const uint32_t x = w ^ 0x88888888u;
         const uint32_t lo = x & 0x0F0F0F0Fu, hi = (x >> 4) & 0x0F0F0F0Fu;
-        const float s = sc.v;
+        const float s = sc.v, zo = sc.zoff;
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-            f[2 * t] = (__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7650u | t)) - 8388616.0f) * s;
-            f[2 * t + 1] = (__uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7650u | t)) - 8388616.0f) * s;
+            f[2 * t] = (__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7650u | t)) - zo) * s;
+            f[2 * t + 1] = (__uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7650u | t)) - zo) * s;
             round2<false>(f[2 * t], f[2 * t + 1]);
         }
     }
@@ -166,7 +181,9 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, MT == 1 ? 4 : 2) gemv_kernel(
                     Scale vc[R];
                     if (INT4 && scaled && p.gb >= 32) {
 #pragma unroll
-                        for (int r = 0; r < R; ++r) vc[r] = prep_scale<BF16>(scale_at(p, gmagic, nr[r], cu * 4), true);
+                        for (int r = 0; r < R; ++r)
+                            vc[r] = prep_scale<BF16>(scale_at(p, gmagic, nr[r], cu * 4), true,
+                                                     zero_at(p, gmagic, nr[r], cu * 4));
                     }
 #pragma unroll
                     for (int j = 0; j < WORDS; ++j) {
@@ -175,9 +192,11 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, MT == 1 ? 4 : 2) gemv_kernel(
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
                             if constexpr (INT4) {
-                                const Scale sc = !scaled ? prep_scale<BF16>(1.0f, false)
-                                                         : (p.gb >= 32 ? vc[r]
-                                                                       : prep_scale<BF16>(scale_at(p, gmagic, nr[r], i8), true));
+                                const Scale sc =
+                                    !scaled ? prep_scale<BF16>(1.0f, false)
+                                            : (p.gb >= 32 ? vc[r]
+                                                          : prep_scale<BF16>(scale_at(p, gmagic, nr[r], i8), true,
+                                                                             zero_at(p, gmagic, nr[r], i8)));
                                 const uint32_t w = j == 0 ? bv[u][r].x : (j == 1 ? bv[u][r].y : (j == 2 ? bv[u][r].z : bv[u][r].w));
                                 dequant8<BF16>(w, sc, b[r]);
                             } else {

@@ -19,9 +19,10 @@ struct GemvParams {
     const void* A;   // M x K, K contiguous (lda elements)
     const void* B;   // N rows of K values, K contiguous: 16-bit (ldb elements) or packed int4 (ldb nibbles)
     const void* V;   // [K / gb][ldv] 16-bit group scales of B, or null
+    const void* Z;   // int4 B with V: [K / gb][ldz] zero points (low nibble of each byte), or null
     const void* C;   // M x N (ldc), read only when beta != 0
     void* D;         // M x N (ldd)
-    int64_t lda, ldb, ldv, ldc, ldd;
+    int64_t lda, ldb, ldv, ldz, ldc, ldd;
     int64_t M, N, K;
     float alpha, beta;
     int32_t a_bf16;  // A (and 16-bit B) is bf16, else fp16

@@ -57,6 +57,7 @@ enum EpiFlags : int32_t { EPI_BIAS = 1, EPI_RELU = 2, EPI_GELU = 4 };
 // copied into the stage by TMA together with the operand tiles.
 struct OperandXform {
     int32_t has_scale;   // scale rows arrive with every stage (TMA), else unscaled
+    int32_t has_zero;    // int4 operand: zero-point rows (one byte per value) arrive too
     int32_t scale_type;  // DT_F16 / DT_BF16
     int32_t group;       // group size along K: a multiple of 64, or a divisor of 64 (>= 8)
     int32_t sc_rows;     // scale rows per 64-wide K-step: max(1, 64 / group)
@@ -113,6 +114,7 @@ QG_HD uint32_t make_idesc_f8(int a_e5m2, int b_e5m2, int m, int n) {
 struct GemmMaps {
     CUtensorMap x, y, c, d;
     CUtensorMap xs, ys;  // scale rows of X / Y (transforming kernel only)
+    CUtensorMap z;       // zero-point rows of the int4 operand (transforming kernel only)
 };
 
 // Per-width launchers (explicitly instantiated in umma_gemm_bn*.cu and

@@ -31,9 +31,17 @@ struct DqCfg {
     static constexpr uint32_t Y_OP = BN * BK * 2;
     static constexpr uint32_t X_RAW = BM * 32;      // packed int4 rows
     static constexpr uint32_t Y_RAW = BN * 32;
-    static constexpr uint32_t X_SC = BM * 2 * 8;    // up to 8 scale rows (group 8) of 16-bit scales
+    // up to 8 scale rows (group 8) of 16-bit scales; the X side's rows are
+    // XS_PITCH wide: a copy starts at the 8-aligned column below the tile's
+    // first row (a grouped problem's token blocks start anywhere), since a
+    // tensor copy's innermost coordinate must be a multiple of 16 bytes
+    static constexpr int XS_PITCH = BM + 8;
+    static constexpr uint32_t X_SC = XS_PITCH * 2 * 8;
     static constexpr uint32_t Y_SC = BN * 2 * 8;
-    static constexpr uint32_t STAGE_BYTES = ((X_OP + Y_OP + X_RAW + Y_RAW + X_SC + Y_SC) + 1023) / 1024 * 1024;
+    static constexpr uint32_t X_ZP = BM * 8;        // up to 8 zero-point rows, one byte per value
+    static constexpr uint32_t Y_ZP = BN * 8;
+    static constexpr uint32_t STAGE_BYTES =
+        ((X_OP + Y_OP + X_RAW + Y_RAW + X_SC + Y_SC + X_ZP + Y_ZP) + 1023) / 1024 * 1024;
     static constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * BN);
     static constexpr uint32_t STAGING_BYTES = EPI_SMEM_BYTES;
     static constexpr int MAX_STAGES = 12;
@@ -76,16 +84,31 @@ struct XformChunks {
 };
 
 // Scale of row r for logical K-chunk j, from the stage's scale rows
-// ([sc_rows][ROWS] 16-bit values; row t covers K-group k0/group + t).  Branch
-// free so the chunks of a thread interleave.
-template <int ROWS>
-__device__ __forceinline__ float stage_scale(const OperandXform& o, const uint8_t* sc, int r, int j) {
+// ([sc_rows][pitch] 16-bit values, the tile's row 0 at column off; row t
+// covers K-group k0/group + t).  Branch free so the chunks of a thread
+// interleave.
+struct ScaleRows {
+    const uint8_t* p;
+    int pitch, off;
+};
+
+__device__ __forceinline__ float stage_scale(const OperandXform& o, const ScaleRows& sc, int r, int j) {
     const int t = o.group >= 64 ? 0 : (8 * j) / o.group;
-    const uint32_t bits = reinterpret_cast<const uint16_t*>(sc)[t * ROWS + r];
+    const uint32_t bits = reinterpret_cast<const uint16_t*>(sc.p)[t * sc.pitch + sc.off + r];
     const float as_f16 = __half2float(__ushort_as_half((unsigned short)bits));
     const float as_bf16 = __uint_as_float(bits << 16);
     const float v = o.scale_type == DT_F16 ? as_f16 : as_bf16;
     return o.has_scale ? v : 1.0f;
+}
+
+// Zero point of row r for logical K-chunk j, from the stage's zero-point rows
+// ([sc_rows][ROWS] bytes, laid out like the scale rows): the two's-complement
+// value of the byte's low nibble; 0 without zero points.
+template <int ROWS>
+__device__ __forceinline__ int stage_zero(const OperandXform& o, const uint8_t* zp, int r, int j) {
+    const int t = o.group >= 64 ? 0 : (8 * j) / o.group;
+    const int z = (int)((uint32_t)zp[t * ROWS + r] << 28) >> 28;
+    return o.has_zero ? z : 0;
 }
 
 template <bool OUT_BF16>
@@ -100,14 +123,15 @@ __device__ __forceinline__ uint32_t pack2t(float a, float b) {
 }
 
 // Transform one operand tile of ROWS rows.  op: the SWIZZLE_128B operand
-// tile; raw: the packed int4 tile (ROWS x 32 bytes); sc: the scale rows.
-// All chunks of a thread are independent; scales and raw words are read
-// first so their shared-memory latency overlaps.
+// tile; raw: the packed int4 tile (ROWS x 32 bytes); sc: the scale rows; zp:
+// the zero-point rows (int4 only).  All chunks of a thread are independent;
+// scales and raw words are read first so their shared-memory latency overlaps.
 template <int ROWS, bool INT4, bool OUT_BF16>
 __device__ __forceinline__ void transform_tile(const OperandXform& o, uint8_t* op, const uint8_t* raw,
-                                               const uint8_t* sc, int tid) {
+                                               const ScaleRows& sc, const uint8_t* zp, int tid) {
     constexpr int NC = XformChunks<ROWS>::N;
     float s[NC];
+    float zoff[NC];  // int4: 2^23 + 8 + z, the bias subtracted from the magic-number float
     uint32_t w[NC];
     uint4 in[NC];
 #pragma unroll
@@ -116,9 +140,11 @@ __device__ __forceinline__ void transform_tile(const OperandXform& o, uint8_t* o
         if (XformChunks<ROWS>::TOTAL % XF_THREADS != 0 && c >= XformChunks<ROWS>::TOTAL) break;
         const int r = c >> 3;
         const int j = INT4 ? (c & 7) : ((c & 7) ^ (r & 7));
-        s[i] = stage_scale<ROWS>(o, sc, r, j);
-        if constexpr (INT4)
+        s[i] = stage_scale(o, sc, r, j);
+        if constexpr (INT4) {
             w[i] = *reinterpret_cast<const uint32_t*>(raw + r * 32 + 4 * (c & 7));
+            zoff[i] = 8388616.0f + (float)stage_zero<ROWS>(o, zp, r, j);  // exact in fp32
+        }
         else
             in[i] = *reinterpret_cast<const uint4*>(op + r * 128 + ((c & 7) << 4));
     }
@@ -130,14 +156,15 @@ __device__ __forceinline__ void transform_tile(const OperandXform& o, uint8_t* o
         uint4 out;
         if constexpr (INT4) {
             // chunk j = c % 8 holds k = k0 + 8j .. +7 (raw bytes 4j .. 4j+3);
-            // biased nibble b = q + 8 becomes the float 2^23 + b, so q = f - (2^23 + 8)
+            // biased nibble b = q + 8 becomes the float 2^23 + b, so
+            // q - z = f - (2^23 + 8 + z), exactly
             const uint32_t x = w[i] ^ 0x88888888u;
             const uint32_t lo = x & 0x0F0F0F0Fu, hi = (x >> 4) & 0x0F0F0F0Fu;
             float q[8];
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
-                q[2 * t] = (__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7650u | t)) - 8388616.0f) * s[i];
-                q[2 * t + 1] = (__uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7650u | t)) - 8388616.0f) * s[i];
+                q[2 * t] = (__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7650u | t)) - zoff[i]) * s[i];
+                q[2 * t + 1] = (__uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7650u | t)) - zoff[i]) * s[i];
             }
             out.x = pack2t<OUT_BF16>(q[0], q[1]);
             out.y = pack2t<OUT_BF16>(q[2], q[3]);
@@ -168,17 +195,20 @@ __device__ __forceinline__ void split_scale_bf16(float v, uint32_t& vhi2, uint32
     vlo2 = (__float_as_uint(vlo) >> 16) * 0x10001u;
 }
 
-// Two int4 values -> RN_bf16(q * v) each, as a bf16 pair.  p holds the even
-// K value's nibble in bits 0-3 and the odd one's in bits 16-19 (other bits
-// ignored).  (b & 0xF) ^ 8 | 0x4300 is the bf16 number 128 + q + 8, so q is
-// exact after subtracting 136; q * vlo is exact in bf16 (<= 7 significant
-// bits), and one fma rounds the exact q * vhi + q * vlo = q * v once.
-__device__ __forceinline__ uint32_t int4_pair_bf16(uint32_t p, uint32_t vhi2, uint32_t vlo2) {
+// Two int4 values -> RN_bf16((q - z) * v) each, as a bf16 pair.  p holds the
+// even K value's nibble in bits 0-3 and the odd one's in bits 16-19 (other
+// bits ignored).  (b & 0xF) ^ 8 | 0x4300 is the bf16 number 128 + q + 8;
+// off2 holds the bf16 number 136 + z twice (128 + 8 + z, exact for a zero
+// point z in [-8, 7]; 136 without one), so q - z is exact after the
+// subtraction; (q - z) * vlo is exact in bf16 (<= 4 + 3 significant bits), and
+// one fma rounds the exact (q - z) * vhi + (q - z) * vlo = (q - z) * v once.
+__device__ __forceinline__ uint32_t int4_off2(int z) { return (0x4300u + (uint32_t)(8 + z)) * 0x10001u; }
+
+__device__ __forceinline__ uint32_t int4_pair_bf16(uint32_t p, uint32_t vhi2, uint32_t vlo2, uint32_t off2) {
     uint32_t m;
     asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(m) : "r"(p), "r"(0x000F000Fu), "r"(0x43084308u));  // (a & b) ^ c
-    const uint32_t off_u = 0x43084308u;  // bf16 136 twice
     const __nv_bfloat162 q2 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&m),
-                                      *reinterpret_cast<const __nv_bfloat162*>(&off_u));
+                                      *reinterpret_cast<const __nv_bfloat162*>(&off2));
     const __nv_bfloat162 r = __hfma2(q2, *reinterpret_cast<const __nv_bfloat162*>(&vhi2),
                                      __hmul2(q2, *reinterpret_cast<const __nv_bfloat162*>(&vlo2)));
     return *reinterpret_cast<const uint32_t*>(&r);
@@ -192,7 +222,7 @@ __device__ __forceinline__ uint32_t int4_pair_bf16(uint32_t p, uint32_t vhi2, ui
 // (RN of the exact product); about 1.7x fewer instructions.
 template <int ROWS>
 __device__ __forceinline__ void transform_int4_bf16_rows(const OperandXform& o, uint8_t* op, const uint8_t* raw,
-                                                         const uint8_t* sc, int tid) {
+                                                         const ScaleRows& sc, const uint8_t* zp, int tid) {
     constexpr int TPR = (XF_THREADS / ROWS) < 2 ? 2 : ((XF_THREADS / ROWS) > 8 ? 8 : (XF_THREADS / ROWS));
     constexpr int CPT = 8 / TPR;                                     // chunks per thread
     constexpr int RPT = (ROWS * TPR + XF_THREADS - 1) / XF_THREADS;  // rows per thread
@@ -215,16 +245,24 @@ __device__ __forceinline__ void transform_int4_bf16_rows(const OperandXform& o, 
             ws[0] = *reinterpret_cast<const uint32_t*>(src);
         }
         uint32_t vhi2 = 0x3F803F80u, vlo2 = 0u;  // unscaled: v = 1
-        if (o.has_scale && !per_chunk) split_scale_bf16(stage_scale<ROWS>(o, sc, r, 0), vhi2, vlo2);
+        uint32_t off2 = int4_off2(0);
+        if (o.has_scale && !per_chunk) {
+            split_scale_bf16(stage_scale(o, sc, r, 0), vhi2, vlo2);
+            off2 = int4_off2(stage_zero<ROWS>(o, zp, r, 0));
+        }
 #pragma unroll
         for (int q = 0; q < CPT; ++q) {
             const int jj = sub * CPT + q;
-            if (per_chunk) split_scale_bf16(stage_scale<ROWS>(o, sc, r, jj), vhi2, vlo2);
+            if (per_chunk) {
+                split_scale_bf16(stage_scale(o, sc, r, jj), vhi2, vlo2);
+                off2 = int4_off2(stage_zero<ROWS>(o, zp, r, jj));
+            }
             const uint32_t w = ws[q], w4 = w >> 4;
             uint32_t out[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t)
-                out[t] = int4_pair_bf16(__byte_perm(w, w4, (uint32_t)t * 0x11u | (uint32_t)(4 + t) * 0x1100u), vhi2, vlo2);
+                out[t] = int4_pair_bf16(__byte_perm(w, w4, (uint32_t)t * 0x11u | (uint32_t)(4 + t) * 0x1100u), vhi2, vlo2,
+                                        off2);
             *reinterpret_cast<uint4*>(op + r * 128 + ((jj ^ (r & 7)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
         }
     }
@@ -232,17 +270,17 @@ __device__ __forceinline__ void transform_int4_bf16_rows(const OperandXform& o, 
 
 template <int ROWS>
 __device__ __forceinline__ void transform_any(const OperandXform& o, uint8_t* op, const uint8_t* raw,
-                                              const uint8_t* sc, int out_bf16, int tid) {
+                                              const ScaleRows& sc, const uint8_t* zp, int out_bf16, int tid) {
     if (o.int4) {
         if (out_bf16)
-            transform_int4_bf16_rows<ROWS>(o, op, raw, sc, tid);
+            transform_int4_bf16_rows<ROWS>(o, op, raw, sc, zp, tid);
         else
-            transform_tile<ROWS, true, false>(o, op, raw, sc, tid);
+            transform_tile<ROWS, true, false>(o, op, raw, sc, zp, tid);
     } else {
         if (out_bf16)
-            transform_tile<ROWS, false, true>(o, op, raw, sc, tid);
+            transform_tile<ROWS, false, true>(o, op, raw, sc, zp, tid);
         else
-            transform_tile<ROWS, false, false>(o, op, raw, sc, tid);
+            transform_tile<ROWS, false, false>(o, op, raw, sc, zp, tid);
     }
 }
 
@@ -251,7 +289,7 @@ __global__ void __launch_bounds__(192 + XF_THREADS, 1)
     umma_dq_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                         const __grid_constant__ CUtensorMap tmXs, const __grid_constant__ CUtensorMap tmYs,
-                        const __grid_constant__ GemmKernelParams P) {
+                        const __grid_constant__ CUtensorMap tmZ, const __grid_constant__ GemmKernelParams P) {
     using Cfg = DqCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -271,8 +309,11 @@ __global__ void __launch_bounds__(192 + XF_THREADS, 1)
     volatile uint32_t* abort_flag = tmem_slot + 2;
 
     const DqParams& dq = P.dq;
-    const uint32_t x_bytes = (dq.x.int4 ? Cfg::X_RAW : Cfg::X_OP) + (dq.x.has_scale ? BM * 2 * dq.x.sc_rows : 0);
-    const uint32_t y_bytes = (dq.y.int4 ? Cfg::Y_RAW : Cfg::Y_OP) + (dq.y.has_scale ? BN * 2 * dq.y.sc_rows : 0);
+    const uint32_t x_bytes = (dq.x.int4 ? Cfg::X_RAW : Cfg::X_OP) +
+                             (dq.x.has_scale ? Cfg::XS_PITCH * 2 * dq.x.sc_rows : 0) +
+                             (dq.x.has_zero ? BM * dq.x.sc_rows : 0);
+    const uint32_t y_bytes = (dq.y.int4 ? Cfg::Y_RAW : Cfg::Y_OP) + (dq.y.has_scale ? BN * 2 * dq.y.sc_rows : 0) +
+                             (dq.y.has_zero ? BN * dq.y.sc_rows : 0);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
@@ -297,6 +338,7 @@ __global__ void __launch_bounds__(192 + XF_THREADS, 1)
         tma_prefetch_desc(&tmY);
         if (P.dq.x.has_scale) tma_prefetch_desc(&tmXs);
         if (P.dq.y.has_scale) tma_prefetch_desc(&tmYs);
+        if (P.dq.x.has_zero || P.dq.y.has_zero) tma_prefetch_desc(&tmZ);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
@@ -318,6 +360,8 @@ __global__ void __launch_bounds__(192 + XF_THREADS, 1)
     auto y_raw = [&](int s) { return x_raw(s) + Cfg::X_RAW; };
     auto x_sc = [&](int s) { return y_raw(s) + Cfg::Y_RAW; };
     auto y_sc = [&](int s) { return x_sc(s) + Cfg::X_SC; };
+    auto x_zp = [&](int s) { return y_sc(s) + Cfg::Y_SC; };
+    auto y_zp = [&](int s) { return x_zp(s) + Cfg::X_ZP; };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -339,15 +383,37 @@ __global__ void __launch_bounds__(192 + XF_THREADS, 1)
                         tma_load_2d(x_raw(s), &tmX, &full[s], k * (BK / 2), (int32_t)u.x_row0);
                     else
                         tma_load_2d(x_op(s), &tmX, &full[s], k * BK, (int32_t)u.x_row0);
-                    if (dq.y.int4)
-                        tma_load_2d(y_raw(s), &tmY, &full[s], k * (BK / 2), (int32_t)u.y_row0);
-                    else
-                        tma_load_2d(y_op(s), &tmY, &full[s], k * BK, (int32_t)u.y_row0);
-                    // the scale rows of this K-step: groups (k*64)/group .. + sc_rows - 1
-                    if (dq.x.has_scale)
-                        tma_load_2d(x_sc(s), &tmXs, &full[s], (int32_t)u.x_row0, (k * BK) / dq.x.group);
-                    if (dq.y.has_scale)
-                        tma_load_2d(y_sc(s), &tmYs, &full[s], (int32_t)u.y_row0, (k * BK) / dq.y.group);
+                    // a grouped problem's Y operand, scales and zero points
+                    // carry the expert as their last coordinate
+                    const int32_t yr = (int32_t)u.y_row0;
+                    if (P.y3d) {
+                        if (dq.y.int4)
+                            tma_load_3d(y_raw(s), &tmY, &full[s], k * (BK / 2), yr, u.batch);
+                        else
+                            tma_load_3d(y_op(s), &tmY, &full[s], k * BK, yr, u.batch);
+                    } else if (dq.y.int4) {
+                        tma_load_2d(y_raw(s), &tmY, &full[s], k * (BK / 2), yr);
+                    } else {
+                        tma_load_2d(y_op(s), &tmY, &full[s], k * BK, yr);
+                    }
+                    // the scale (and zero-point) rows of this K-step: groups
+                    // (k*64)/group .. + sc_rows - 1
+                    if (dq.x.has_scale)  // from the 8-aligned column at or below the tile's first row
+                        tma_load_2d(x_sc(s), &tmXs, &full[s], (int32_t)(u.x_row0 & ~int64_t(7)), (k * BK) / dq.x.group);
+                    if (dq.x.has_zero)
+                        tma_load_2d(x_zp(s), &tmZ, &full[s], (int32_t)u.x_row0, (k * BK) / dq.x.group);
+                    if (dq.y.has_scale) {
+                        if (P.y3d)
+                            tma_load_3d(y_sc(s), &tmYs, &full[s], yr, (k * BK) / dq.y.group, u.batch);
+                        else
+                            tma_load_2d(y_sc(s), &tmYs, &full[s], yr, (k * BK) / dq.y.group);
+                    }
+                    if (dq.y.has_zero) {
+                        if (P.y3d)
+                            tma_load_3d(y_zp(s), &tmZ, &full[s], yr, (k * BK) / dq.y.group, u.batch);
+                        else
+                            tma_load_2d(y_zp(s), &tmZ, &full[s], yr, (k * BK) / dq.y.group);
+                    }
                     armed |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
                     if (++s == S) {
@@ -420,8 +486,11 @@ __global__ void __launch_bounds__(192 + XF_THREADS, 1)
                     ok = false;
                     break;
                 }
-                if (dq.x.active) transform_any<BM>(dq.x, x_op(s), x_raw(s), x_sc(s), dq.out_bf16, tid);
-                if (dq.y.active) transform_any<BN>(dq.y, y_op(s), y_raw(s), y_sc(s), dq.out_bf16, tid);
+                if (dq.x.active)
+                    transform_any<BM>(dq.x, x_op(s), x_raw(s), ScaleRows{x_sc(s), Cfg::XS_PITCH, (int)(u.x_row0 & 7)},
+                                      x_zp(s), dq.out_bf16, tid);
+                if (dq.y.active)
+                    transform_any<BN>(dq.y, y_op(s), y_raw(s), ScaleRows{y_sc(s), BN, 0}, y_zp(s), dq.out_bf16, tid);
                 // each thread orders its generic-proxy writes before the
                 // tensor core's reads; the warp then arrives once
                 fence_proxy_async_smem();
@@ -459,7 +528,8 @@ cudaError_t launch_dq_bn(const GemmMaps& m, const GemmKernelParams& p, int grid,
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
-    return launch_pdl(umma_dq_gemm_kernel<BN>, grid, 192 + XF_THREADS, smem, st, m.x, m.y, m.c, m.d, m.xs, m.ys, p);
+    return launch_pdl(umma_dq_gemm_kernel<BN>, grid, 192 + XF_THREADS, smem, st, m.x, m.y, m.c, m.d, m.xs, m.ys, m.z,
+                      p);
 }
 
 template <int BN>

@@ -195,6 +195,36 @@ class GroupedProblem:
     bias_type: int | None = None
     q_scale: np.ndarray | None = None
     q_zp: int = 0
+    b_type: int | None = None    # None: same as a_type; S4 for int4 experts
+    V: np.ndarray | None = None  # [E, K/gb, N] per-expert scales
+    v_type: int | None = None
+    gb: int = 0
+    Z: np.ndarray | None = None  # [E, K/gb, N] int8 zero points (int4 B with V)
+    U: np.ndarray | None = None  # [K/ga, sum m_e] per-token scales
+    u_type: int | None = None
+    ga: int = 0
+
+
+def grouped_w4a16(counts, N, K, *, seed, group=128, a_type=BF16, zero=False, vlo=0.005, vhi=0.02,
+                  name="") -> GroupedProblem:
+    """Grouped problem with int4 experts: A ~ N(0,1) [sum m_e, K], B int4 uniform
+    in [-8, 7] packed [E, N, K/2], V fp16 uniform[vlo, vhi] per (expert, group,
+    column), and with zero=True integer zero points uniform in [-8, 7]."""
+    counts = np.asarray(counts, dtype=np.int64)
+    E = len(counts)
+    g = _rng(seed)
+    T = int(counts.sum())
+    a = g.standard_normal(size=(T, K), dtype=np.float32)
+    q = g.integers(-8, 8, size=(E, N, K), dtype=np.int64)
+    v = g.uniform(vlo, vhi, size=(E, K // group, N)).astype(np.float32)
+    off = np.zeros(E + 1, dtype=np.int32)
+    off[1:] = np.cumsum(counts)
+    gp = GroupedProblem(counts, off, N, K, a_type, BF16, _round_bits(a, a_type), pack_int4(q),
+                        name=name or f"grouped W4A16 {E}x{N}x{K}", b_type=S4, V=_round_bits(v, F16), v_type=F16,
+                        gb=group)
+    if zero:
+        gp.Z = g.integers(-8, 8, size=(E, K // group, N), dtype=np.int64).astype(np.int8)
+    return gp
 
 
 def grouped(counts, N, K, *, seed, a_type=BF16, d_type=BF16, a_scale=1.0, b_scale=0.02,

@@ -45,6 +45,17 @@ def padded_rows(bits, dtype):
     return t, ld
 
 
+def zero_rows(Z):
+    """int8 zero points [.., rows, cols] on the device with the row stride
+    rounded up to 16 bytes; returns (tensor, ld, batch stride in bytes)."""
+    Z = np.ascontiguousarray(Z, dtype=np.int8)
+    lead, (rows, cols) = Z.shape[:-2], Z.shape[-2:]
+    ld = -(-cols // 16) * 16
+    t = torch.zeros(*lead, rows, ld, dtype=torch.int8, device="cuda")
+    t[..., :cols] = torch.from_numpy(Z).cuda()
+    return t, ld, rows * ld
+
+
 def tolerance(ref, bound, d_type):
     tol = 1e-5 * bound + 1e-6
     if d_type != synth.F32:
@@ -124,6 +135,10 @@ def run_problem(lib, p, o=None, D=None, C=None, stream=None, workspace=True):
         V, ldv = padded_rows(p.V, p.v_type)
         Vd = qg.layout(p.v_type, qg.GEMM_ROW_MAJOR, p.K // p.gb, p.N, ldv)
     bias = _attach_epilogue(p, o)
+    Z = None
+    if getattr(p, "Z", None) is not None:
+        Z, o.b_zero_ld, _ = zero_rows(p.Z)
+        o.b_zero = qg.ptr(Z)
     qs = None
     if p.d_type == synth.S8:
         qs = torch.from_numpy(np.ascontiguousarray(p.q_scale, dtype=np.float32)).cuda()
@@ -151,29 +166,50 @@ def _attach_epilogue(p, o):
 
 
 def grouped_to_device(gp):
+    b_type = getattr(gp, "b_type", None)
+    b_type = gp.a_type if b_type is None else b_type
     A = dev_bits(gp.A, gp.a_type)
-    B = dev_bits(gp.B, gp.a_type)
+    B = dev_bits(gp.B, b_type)
     off = torch.from_numpy(gp.offsets.astype(np.int32)).cuda()
     return A, B, off
 
 
 def run_grouped(lib, gp, o=None, A=None, B=None, off=None):
+    """Run a synth.GroupedProblem through gemm_run_grouped (with its per-token
+    U, per-expert V and zero points when it has them).  Returns (status, D)."""
     if A is None:
         A, B, off = grouped_to_device(gp)
     T = int(gp.offsets[-1])
+    E = len(gp.counts)
     fill = 101 if gp.d_type == synth.S8 else float("nan")
     D = torch.full((T, gp.N), fill, dtype=TORCH_DT[gp.d_type], device="cuda")
-    o = o or op()
+    o = o or op(ga=getattr(gp, "ga", 0) if getattr(gp, "U", None) is not None else 0,
+                gb=getattr(gp, "gb", 0) if getattr(gp, "V", None) is not None else 0)
+    b_type = getattr(gp, "b_type", None)
+    Bd = qg.col_major_from_nk(B, k=gp.K, type_=gp.a_type if b_type is None else b_type)
+    U = Ud = V = Vd = Z = None
+    if getattr(gp, "U", None) is not None:
+        U, ldu = padded_rows(gp.U, gp.u_type)
+        Ud = qg.layout(gp.u_type, qg.GEMM_ROW_MAJOR, gp.K // gp.ga, T, ldu)
+    if getattr(gp, "V", None) is not None:
+        groups = gp.K // gp.gb
+        ldv = -(-gp.N // 8) * 8
+        V = torch.zeros(E, groups, ldv, dtype=TORCH_DT[gp.v_type], device="cuda")
+        V[..., :gp.N] = dev_bits(gp.V, gp.v_type)
+        Vd = qg.layout(gp.v_type, qg.GEMM_ROW_MAJOR, groups, gp.N, ldv, E, groups * ldv)
+    if getattr(gp, "Z", None) is not None:
+        Z, o.b_zero_ld, o.b_zero_batch_stride = zero_rows(gp.Z)
+        o.b_zero = qg.ptr(Z)
     bias = _attach_epilogue(gp, o)
     qs = None
     if gp.d_type == synth.S8:
         qs = torch.from_numpy(np.ascontiguousarray(gp.q_scale, dtype=np.float32)).cuda()
         o.out_scale, o.out_zero_point = qg.ptr(qs), gp.q_zp
-    rc = qg.gemm_run_grouped(lib.h, o, gp.alpha, qg.ptr(A), qg.row_major(A), None, None, qg.ptr(B),
-                             qg.col_major_from_nk(B), None, None, gp.beta, None, None, qg.ptr(D), qg.row_major(D),
-                             qg.ptr(off), len(gp.counts), lib.ws.c, qg.current_stream())
+    rc = qg.gemm_run_grouped(lib.h, o, gp.alpha, qg.ptr(A), qg.row_major(A), qg.ptr(U), Ud, qg.ptr(B), Bd, qg.ptr(V),
+                             Vd, gp.beta, None, None, qg.ptr(D), qg.row_major(D), qg.ptr(off), E, lib.ws.c,
+                             qg.current_stream())
     torch.cuda.synchronize()
-    del bias, qs
+    del bias, qs, U, V, Z
     return rc, D
 
 

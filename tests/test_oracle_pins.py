@@ -544,3 +544,21 @@ def test_zero_points_of_zero_are_symmetric():
     p.Z = None
     r2, b2 = oracle.gemm(p)
     assert np.array_equal(r1, r2) and np.array_equal(b1, b2)
+
+
+def test_grouped_w4a16_matches_numpy_per_expert():
+    # per-expert V and zero points: each expert's b-hat rounded by torch from
+    # the exact fp32 product, then a numpy float64 matmul per expert
+    gp = synth.grouped_w4a16([5, 0, 17, 9], 24, 256, seed=36, group=64, zero=True)
+    ref, bound = oracle.grouped(gp)
+    a = lib_decode(BF16, gp.A)
+    for e in range(4):
+        lo, hi = int(gp.offsets[e]), int(gp.offsets[e + 1])
+        if hi == lo:
+            continue
+        q = oracle.unpack_int4(gp.B[e]).astype(np.float32)                       # N x K
+        z = gp.Z[e].astype(np.float32)[np.arange(256) // 64, :].T
+        v = lib_decode(F16, gp.V[e]).astype(np.float32)[np.arange(256) // 64, :].T
+        bhat = torch.from_numpy((q - z) * v).to(torch.bfloat16).to(torch.float64).numpy()
+        np.testing.assert_allclose(ref[lo:hi], a[lo:hi] @ bhat.T, rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(bound[lo:hi], np.abs(a[lo:hi]) @ np.abs(bhat.T), rtol=1e-13, atol=1e-13)
