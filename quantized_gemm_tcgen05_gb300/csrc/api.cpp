@@ -557,6 +557,10 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
         }
         kp.stages = umma_dq_max_stages(c.bn);
         if (kp.stages < 2) return GEMM_ERR_NO_KERNEL;
+        if (const char* fs = getenv("GEMM_STAGES")) {  // ring depth override for tuning sweeps
+            const int want = atoi(fs);
+            if (want >= 2 && want < kp.stages) kp.stages = want;
+        }
         cudaError_t ce = launch_umma_dq_gemm(c.bn, maps, kp, kp.sched.programs, st);
         return ce == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }

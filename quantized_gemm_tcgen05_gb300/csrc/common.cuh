@@ -464,12 +464,13 @@ __device__ __forceinline__ bool final_unit(const GemmKernelParams& P, WorkIter w
 // The last arriver of a split tile copies every contributor's partial tile
 // (BM x BN fp32, contiguous per slot) into the idle ring with bulk copies --
 // all in flight at once instead of a few loads per thread -- and waits for
-// them.  Called by all epilogue threads; returns false if the wait gave up.
+// them.  Called by all epilogue threads (lead: the first of them); returns
+// false if the wait gave up.
 template <int BN>
 __device__ __forceinline__ bool fixup_bulk_load(const GemmKernelParams& P, const Unit& u, const FixupSmem& fx,
-                                                const Guard& g) {
+                                                const Guard& g, int lead) {
     constexpr uint32_t TILE_BYTES = BM * BN * 4;
-    if (threadIdx.x == 64) {
+    if ((int)threadIdx.x == lead) {
         fence_proxy_async_global();  // the contributors' partial stores -> our bulk reads
         mbar_arrive_expect_tx(fx.bar, (uint32_t)u.ncontrib * TILE_BYTES);
         for (int q = 0; q < u.ncontrib; ++q)
@@ -485,13 +486,15 @@ __device__ __forceinline__ bool fixup_fits(const FixupSmem& fx, const Unit& u) {
     return fx.base != nullptr && (uint64_t)u.ncontrib * BM * BN * 4 <= fx.bytes;
 }
 
-// The epilogue role: 4 warps (128 threads), warp w reads TMEM lanes
-// 32*(w%4) .. 32*(w%4)+31.  For every unit: wait for the accumulator, then
-// either store it (whole tile) or write it as a partial and, if this unit is
-// the last of its tile to arrive, reduce all partials in K order and store.
+// The epilogue role: 4 warps (128 threads, the first of them `lead`), warp w
+// reads TMEM lanes 32*(w%4) .. 32*(w%4)+31.  For every unit: wait for the
+// accumulator, then either store it (whole tile) or write it as a partial
+// and, if this unit is the last of its tile to arrive, reduce all partials in
+// K order and store.
 template <int BN>
 __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uint64_t* tfull, uint64_t* tempty,
-                              float* staging_all, volatile uint32_t* bcast, const FixupSmem& fx, const Guard& g) {
+                              float* staging_all, volatile uint32_t* bcast, const FixupSmem& fx, const Guard& g,
+                              int lead) {
     using CK = Chunk<BN>;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int ew = warp % 4;
@@ -544,7 +547,7 @@ __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uin
         mbar_arrive(&tempty[buf]);
         __threadfence();
         epi_bar_sync();
-        if (threadIdx.x == 64) {
+        if ((int)threadIdx.x == lead) {
             const int old = atomicAdd(tile_counter(P, u.tile), 1);
             const bool last = (old == u.ncontrib - 1);
             if (last) atomicExch(tile_counter(P, u.tile), 0);  // every contributor has arrived
@@ -554,7 +557,7 @@ __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uin
         if (*bcast == 0u) continue;
         __threadfence();
         const bool bulk = fixup_fits<BN>(fx, u) && final_unit(P, w, BN);
-        if (bulk && !fixup_bulk_load<BN>(P, u, fx, g)) break;
+        if (bulk && !fixup_bulk_load<BN>(P, u, fx, g, lead)) break;
 #pragma unroll 1
         for (int c = 0; c < CK::N; ++c) {
             CChunk<CK::W> cc;
@@ -643,7 +646,8 @@ struct ChunkStream {
 template <int BN>
 __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, const CUtensorMap* tmD,
                              uint32_t tmem_base, uint64_t* tfull, uint64_t* tempty, uint8_t* ebuf_all,
-                             uint64_t* cbar_all, volatile uint32_t* bcast, const FixupSmem& fx, const Guard& g) {
+                             uint64_t* cbar_all, volatile uint32_t* bcast, const FixupSmem& fx, const Guard& g,
+                             int lead) {
     constexpr int W = 32;
     constexpr int NCH = BN / W;
     const EpiParams& e = P.epi;
@@ -839,7 +843,7 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
         mbar_arrive(&tempty[buf]);
         __threadfence();
         epi_bar_sync();
-        if (threadIdx.x == 64) {
+        if ((int)threadIdx.x == lead) {
             const int old = atomicAdd(tile_counter(P, u.tile), 1);
             const bool last = (old == u.ncontrib - 1);
             if (last) atomicExch(tile_counter(P, u.tile), 0);
@@ -849,7 +853,7 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
         const bool last = *bcast != 0u;
         if (last) __threadfence();
         const bool bulk = last && fixup_fits<BN>(fx, u) && final_unit(P, w, BN);
-        if (bulk && !fixup_bulk_load<BN>(P, u, fx, g)) break;
+        if (bulk && !fixup_bulk_load<BN>(P, u, fx, g, lead)) break;
 #pragma unroll 1
         for (int c = 0; c < NCH && ok; ++c) {
             float v[W];
@@ -910,18 +914,20 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
     __syncwarp();
 }
 
+// The epilogue of a kernel whose epilogue warps are the four starting at
+// thread `lead` (a multiple of 128 plus, in the two-role kernels, 64).
 template <int BN>
 __device__ __forceinline__ void epilogue(const GemmKernelParams& P, const CUtensorMap* tmC, const CUtensorMap* tmD,
                                          uint32_t tmem_base, uint64_t* tfull, uint64_t* tempty, uint8_t* esmem,
                                          uint64_t* cbar, volatile uint32_t* bcast, const FixupSmem& fx,
-                                         const Guard& g) {
+                                         const Guard& g, int lead) {
     if constexpr (BN >= 32) {
         if (P.epi.tma) {
-            epilogue_tma<BN>(P, tmC, tmD, tmem_base, tfull, tempty, esmem, cbar, bcast, fx, g);
+            epilogue_tma<BN>(P, tmC, tmD, tmem_base, tfull, tempty, esmem, cbar, bcast, fx, g, lead);
             return;
         }
     }
-    epilogue_role<BN>(P, tmem_base, tfull, tempty, reinterpret_cast<float*>(esmem), bcast, fx, g);
+    epilogue_role<BN>(P, tmem_base, tfull, tempty, reinterpret_cast<float*>(esmem), bcast, fx, g, lead);
 }
 
 }  // namespace qg

@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(192 + XF_THREADS, 1)
         }
     } else if (warp < 6) {
         const FixupSmem fx{ring, (uint32_t)((size_t)S * Cfg::STAGE_BYTES), fixbar};
-        epilogue<BN>(P, &tmC, &tmD, tmem_base, tfull, tempty, reinterpret_cast<uint8_t*>(staging), cbar, bcast, fx, g);
+        epilogue<BN>(P, &tmC, &tmD, tmem_base, tfull, tempty, reinterpret_cast<uint8_t*>(staging), cbar, bcast, fx, g, 64);
     } else {
         // transform warps
         const int tid = threadIdx.x - 192;

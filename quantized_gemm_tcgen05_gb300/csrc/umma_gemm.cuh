@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else {
         const FixupSmem fx{ring, (uint32_t)((size_t)S * stage_bytes), fixbar};
-        epilogue<BN>(P, &tmC, &tmD, tmem_base, tfull, tempty, reinterpret_cast<uint8_t*>(staging), cbar, bcast, fx, g);
+        epilogue<BN>(P, &tmC, &tmD, tmem_base, tfull, tempty, reinterpret_cast<uint8_t*>(staging), cbar, bcast, fx, g, 64);
     }
 
     tc_fence_before_sync();
