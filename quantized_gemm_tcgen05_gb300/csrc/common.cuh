@@ -23,6 +23,7 @@ constexpr int UMMA_K = 16;
 // per-warp C/D tile buffers (TMA path), whichever the launch uses.
 constexpr uint32_t EPI_SMEM_BYTES = 32 * 1024;
 constexpr int EPI_CBARS = 16;  // 4 epilogue warps x up to 4 buffers
+constexpr int FIX_BARS = 4;    // completion barriers of the split-tile reduction's bulk copies
 
 // TMEM is allocated in power-of-two column counts of at least 32.
 __host__ __device__ constexpr uint32_t tmem_cols_for(uint32_t cols) {
@@ -443,7 +444,7 @@ __device__ __forceinline__ float4* partial_quad(float* partials, int64_t slot, i
 struct FixupSmem {
     uint8_t* base;
     uint32_t bytes;
-    uint64_t* bar;  // completion barrier of the bulk copies (used at most once)
+    uint64_t* bar;  // FIX_BARS completion barriers of the bulk copies (used on the final unit only)
 };
 
 // The CTA pair splits every tile into two 128-row halves, one per CTA, each
@@ -461,29 +462,89 @@ __device__ __forceinline__ bool final_unit(const GemmKernelParams& P, WorkIter w
     return !next_unit(P, w, u2, bn);
 }
 
-// The last arriver of a split tile copies every contributor's partial tile
-// (BM x BN fp32, contiguous per slot) into the idle ring with bulk copies --
-// all in flight at once instead of a few loads per thread -- and waits for
-// them.  Called by all epilogue threads (lead: the first of them); returns
-// false if the wait gave up.
-template <int BN>
-__device__ __forceinline__ bool fixup_bulk_load(const GemmKernelParams& P, const Unit& u, const FixupSmem& fx,
-                                                const Guard& g, int lead) {
-    constexpr uint32_t TILE_BYTES = BM * BN * 4;
+// Arrival of a split tile's contributor, after its partial tile is written:
+// one CTA barrier orders every epilogue thread's partial stores before the
+// lead thread's release fence and counter increment (the fence is cumulative),
+// so one thread pays the write-acknowledgement latency instead of each.  The
+// last arriver resets the counter and acquires the others' partials.  Returns
+// whether this unit's CTA is the tile's last arriver (every epilogue thread).
+__device__ __forceinline__ bool split_arrive(const GemmKernelParams& P, const Unit& u, volatile uint32_t* bcast,
+                                             int lead) {
+    epi_bar_sync();
     if ((int)threadIdx.x == lead) {
-        fence_proxy_async_global();  // the contributors' partial stores -> our bulk reads
-        mbar_arrive_expect_tx(fx.bar, (uint32_t)u.ncontrib * TILE_BYTES);
-        for (int q = 0; q < u.ncontrib; ++q)
-            bulk_load_g2s(fx.base + (size_t)q * TILE_BYTES,
-                          P.partials + half_slot(P, partial_slot(P.sched, u.tile, q)) * (int64_t)(BM * BN), TILE_BYTES,
-                          fx.bar);
+        __threadfence();
+        const int old = atomicAdd(tile_counter(P, u.tile), 1);
+        const bool last = (old == u.ncontrib - 1);
+        if (last) {
+            atomicExch(tile_counter(P, u.tile), 0);  // every contributor has arrived
+            __threadfence();
+        }
+        *bcast = last ? 1u : 0u;
     }
-    return __all_sync(0xffffffffu, wait_bar(fx.bar, 0, g, SITE_EPI_TMEM_FULL));
+    epi_bar_sync();
+    return *bcast != 0u;
 }
 
+// Chunks of a split tile's partials that the idle ring can hold at once for
+// all contributors (0: the bulk path does not fit).
 template <int BN>
-__device__ __forceinline__ bool fixup_fits(const FixupSmem& fx, const Unit& u) {
-    return fx.base != nullptr && (uint64_t)u.ncontrib * BM * BN * 4 <= fx.bytes;
+__device__ __forceinline__ int fixup_buffers(const FixupSmem& fx, const Unit& u) {
+    constexpr uint32_t CHUNK = BM * Chunk<BN>::W * 4;
+    if (fx.base == nullptr) return 0;
+    const uint32_t n = fx.bytes / ((uint32_t)u.ncontrib * CHUNK);
+    return (int)(n < (uint32_t)FIX_BARS ? (n < (uint32_t)Chunk<BN>::N ? n : Chunk<BN>::N)
+                                        : ((uint32_t)FIX_BARS < (uint32_t)Chunk<BN>::N ? FIX_BARS : Chunk<BN>::N));
+}
+
+// The last arriver's reduction on its final unit: column chunk c of every
+// contributor's partial tile (BM x W fp32, contiguous in a slot) is copied
+// into the idle ring with bulk copies, nbuf chunks in flight at once, each
+// chunk completing on its own barrier; the epilogue sums a chunk over the
+// contributors in K order (fixup_reduce) while the next chunks land.
+// fixup_issue(c): the lead thread starts chunk c's copies.
+template <int BN>
+__device__ __forceinline__ void fixup_issue(const GemmKernelParams& P, const Unit& u, const FixupSmem& fx, int lead,
+                                            int nbuf, int c) {
+    using CK = Chunk<BN>;
+    constexpr uint32_t CHUNK = BM * CK::W * 4;
+    if ((int)threadIdx.x != lead || c >= CK::N) return;
+    const uint32_t per = (uint32_t)u.ncontrib * CHUNK;
+    if (c == 0) fence_proxy_async_global();  // the contributors' partial stores -> bulk reads
+    uint64_t* bar = &fx.bar[c % nbuf];
+    mbar_arrive_expect_tx(bar, per);
+    for (int q = 0; q < u.ncontrib; ++q)
+        bulk_load_g2s(fx.base + (size_t)(c % nbuf) * per + (size_t)q * CHUNK,
+                      P.partials + half_slot(P, partial_slot(P.sched, u.tile, q)) * (int64_t)(BM * BN) +
+                          (int64_t)c * (BM * CK::W),
+                      CHUNK, bar);
+}
+
+// Sum chunk c of every contributor into v (zeroed by the caller), in K order,
+// once its copies have landed; then, after every epilogue thread is done with
+// the buffer, start chunk c + nbuf in it.  Returns false if the wait gave up.
+template <int BN>
+__device__ __forceinline__ bool fixup_reduce(const GemmKernelParams& P, const Unit& u, const FixupSmem& fx,
+                                             const Guard& g, int lead, int nbuf, int c, float (&v)[Chunk<BN>::W]) {
+    using CK = Chunk<BN>;
+    constexpr uint32_t CHUNK = BM * CK::W * 4;
+    if (!__all_sync(0xffffffffu, wait_bar(&fx.bar[c % nbuf], (uint32_t)(c / nbuf) & 1u, g, SITE_EPI_TMEM_FULL)))
+        return false;
+    const int r = (int)(threadIdx.x % 128);
+    const float4* src = reinterpret_cast<const float4*>(fx.base + (size_t)(c % nbuf) * u.ncontrib * CHUNK);
+#pragma unroll 1
+    for (int q = 0; q < u.ncontrib; ++q) {
+#pragma unroll
+        for (int j = 0; j < CK::Q; ++j) {
+            const float4 p = src[(size_t)q * (CK::Q * BM) + j * BM + r];
+            v[4 * j] += p.x;
+            v[4 * j + 1] += p.y;
+            v[4 * j + 2] += p.z;
+            v[4 * j + 3] += p.w;
+        }
+    }
+    epi_bar_sync();  // every thread is done with this buffer before it is refilled
+    fixup_issue<BN>(P, u, fx, lead, nbuf, c + nbuf);
+    return true;
 }
 
 // The epilogue role: 4 warps (128 threads, the first of them `lead`), warp w
@@ -545,19 +606,11 @@ __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uin
         }
         tc_fence_before_sync();
         mbar_arrive(&tempty[buf]);
-        __threadfence();
-        epi_bar_sync();
-        if ((int)threadIdx.x == lead) {
-            const int old = atomicAdd(tile_counter(P, u.tile), 1);
-            const bool last = (old == u.ncontrib - 1);
-            if (last) atomicExch(tile_counter(P, u.tile), 0);  // every contributor has arrived
-            *bcast = last ? 1u : 0u;
-        }
-        epi_bar_sync();
-        if (*bcast == 0u) continue;
-        __threadfence();
-        const bool bulk = fixup_fits<BN>(fx, u) && final_unit(P, w, BN);
-        if (bulk && !fixup_bulk_load<BN>(P, u, fx, g, lead)) break;
+        if (!split_arrive(P, u, bcast, lead)) continue;
+        // on the final unit the idle ring takes the contributors' partials, chunk by chunk
+        const int nbuf = final_unit(P, w, BN) ? fixup_buffers<BN>(fx, u) : 0;
+        for (int c = 0; c < nbuf; ++c) fixup_issue<BN>(P, u, fx, lead, nbuf, c);
+        bool fix_ok = true;
 #pragma unroll 1
         for (int c = 0; c < CK::N; ++c) {
             CChunk<CK::W> cc;
@@ -565,19 +618,10 @@ __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uin
             float v[CK::W];
 #pragma unroll
             for (int i = 0; i < CK::W; ++i) v[i] = 0.0f;
-            if (bulk) {
-                // contributors in K order, from the ring
-#pragma unroll 1
-                for (int q = 0; q < u.ncontrib; ++q) {
-                    const float4* src = reinterpret_cast<const float4*>(fx.base + (size_t)q * (BM * BN * 4));
-#pragma unroll
-                    for (int j = 0; j < CK::Q; ++j) {
-                        const float4 p = src[(c * CK::Q + j) * BM + r];
-                        v[4 * j] += p.x;
-                        v[4 * j + 1] += p.y;
-                        v[4 * j + 2] += p.z;
-                        v[4 * j + 3] += p.w;
-                    }
+            if (nbuf > 0) {
+                if (!fixup_reduce<BN>(P, u, fx, g, lead, nbuf, c, v)) {
+                    fix_ok = false;
+                    break;
                 }
                 store_chunk<CK::W>(P.epi, u, ew, lane, c * CK::W, v, cc, staging);
                 continue;
@@ -613,6 +657,7 @@ __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uin
             }
             store_chunk<CK::W>(P.epi, u, ew, lane, c * CK::W, v, cc, staging);
         }
+        if (!fix_ok) break;
     }
 }
 
@@ -841,37 +886,19 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
         }
         tc_fence_before_sync();
         mbar_arrive(&tempty[buf]);
-        __threadfence();
-        epi_bar_sync();
-        if ((int)threadIdx.x == lead) {
-            const int old = atomicAdd(tile_counter(P, u.tile), 1);
-            const bool last = (old == u.ncontrib - 1);
-            if (last) atomicExch(tile_counter(P, u.tile), 0);
-            *bcast = last ? 1u : 0u;
-        }
-        epi_bar_sync();
-        const bool last = *bcast != 0u;
-        if (last) __threadfence();
-        const bool bulk = last && fixup_fits<BN>(fx, u) && final_unit(P, w, BN);
-        if (bulk && !fixup_bulk_load<BN>(P, u, fx, g, lead)) break;
+        const bool last = split_arrive(P, u, bcast, lead);
+        // on the final unit the idle ring takes the contributors' partials, chunk by chunk
+        const int nbuf = last && final_unit(P, w, BN) ? fixup_buffers<BN>(fx, u) : 0;
+        for (int c = 0; c < nbuf; ++c) fixup_issue<BN>(P, u, fx, lead, nbuf, c);
 #pragma unroll 1
         for (int c = 0; c < NCH && ok; ++c) {
             float v[W];
 #pragma unroll
             for (int i = 0; i < W; ++i) v[i] = 0.0f;
-            if (bulk) {
-                // contributors in K order, from the ring
-#pragma unroll 1
-                for (int q = 0; q < u.ncontrib; ++q) {
-                    const float4* src = reinterpret_cast<const float4*>(fx.base + (size_t)q * (BM * BN * 4));
-#pragma unroll
-                    for (int j = 0; j < W / 4; ++j) {
-                        const float4 p = src[(c * (W / 4) + j) * BM + r];
-                        v[4 * j] += p.x;
-                        v[4 * j + 1] += p.y;
-                        v[4 * j + 2] += p.z;
-                        v[4 * j + 3] += p.w;
-                    }
+            if (nbuf > 0) {
+                if (!fixup_reduce<BN>(P, u, fx, g, lead, nbuf, c, v)) {
+                    ok = false;
+                    break;
                 }
             } else if (last) {
 #pragma unroll 1

@@ -45,7 +45,7 @@ struct DqCfg {
     static constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * BN);
     static constexpr uint32_t STAGING_BYTES = EPI_SMEM_BYTES;
     static constexpr int MAX_STAGES = 12;
-    static constexpr uint32_t AUX_BYTES = (3 * MAX_STAGES + 6 + EPI_CBARS) * 8 + 16;
+    static constexpr uint32_t AUX_BYTES = (3 * MAX_STAGES + 5 + FIX_BARS + EPI_CBARS) * 8 + 16;
     static constexpr uint32_t FIXED_BYTES = 1024 + STAGING_BYTES + AUX_BYTES;
     static size_t smem_bytes(int stages) { return FIXED_BYTES + (size_t)stages * STAGE_BYTES; }
     static int max_stages() {
@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(192 + XF_THREADS, 1)
     uint64_t* done = tempty + 2;
     uint64_t* cbar = done + 1;
     uint64_t* fixbar = cbar + EPI_CBARS;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fixbar + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fixbar + FIX_BARS);
     volatile uint32_t* bcast = tmem_slot + 1;
     volatile uint32_t* abort_flag = tmem_slot + 2;
 
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(192 + XF_THREADS, 1)
         }
         mbar_init(done, 1);
         for (int i = 0; i < EPI_CBARS; ++i) mbar_init(&cbar[i], 1);
-        mbar_init(fixbar, 1);
+        for (int i = 0; i < FIX_BARS; ++i) mbar_init(&fixbar[i], 1);
         *bcast = 0;
         *abort_flag = 0;
         fence_barrier_init();

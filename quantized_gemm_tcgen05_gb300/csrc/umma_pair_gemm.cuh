@@ -40,7 +40,7 @@ struct PairCfg {
     // the epilogue keeps two C/D buffers per warp (16-bit D; fp32 D uses the
     // register path), leaving room for one more ring stage
     static constexpr uint32_t EPI_BYTES = EPI_SMEM_BYTES / 2;
-    static constexpr uint32_t AUX_BYTES = (2 * MAX_STAGES + 8 + EPI_CBARS) * 8 + 16;
+    static constexpr uint32_t AUX_BYTES = (2 * MAX_STAGES + 7 + FIX_BARS + EPI_CBARS) * 8 + 16;
     static constexpr uint32_t FIXED_BYTES = 1024 + EPI_BYTES + AUX_BYTES;
     // a stage holds ks 64-wide K-steps of both operands
     static size_t smem_bytes(int stages, int ks) { return FIXED_BYTES + (size_t)stages * ks * STAGE_BYTES; }
@@ -88,7 +88,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     uint64_t* done = ptempty + 2;
     uint64_t* cbar = done + 1;
     uint64_t* fixbar = cbar + EPI_CBARS;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fixbar + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fixbar + FIX_BARS);
     volatile uint32_t* bcast = tmem_slot + 1;
     volatile uint32_t* abort_flag = tmem_slot + 2;
 
@@ -107,7 +107,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         }
         mbar_init(done, 1);
         for (int i = 0; i < EPI_CBARS; ++i) mbar_init(&cbar[i], 1);
-        mbar_init(fixbar, 1);
+        for (int i = 0; i < FIX_BARS; ++i) mbar_init(&fixbar[i], 1);
         *bcast = 0;
         *abort_flag = 0;
         fence_barrier_init();
