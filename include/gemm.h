@@ -47,7 +47,8 @@ typedef enum {
     GEMM_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed               */
     GEMM_ERR_NO_KERNEL = 5,      /* no registered kernel accepts the problem        */
     GEMM_ERR_DEVICE_TIMEOUT = 6, /* a kernel gave up on a bounded wait             */
-    GEMM_ERR_BAD_CACHE = 7       /* import blob malformed, wrong version or device  */
+    GEMM_ERR_BAD_CACHE = 7,      /* import blob malformed, wrong version or device  */
+    GEMM_ERR_DEVICE_CHECK = 8    /* a device-side bounds check failed (checked build) */
 } gemm_status_t;
 
 /* ---- operand description ------------------------------------------------------ */
@@ -295,13 +296,25 @@ int gemm_cache_size(gemm_handle_t h, int32_t* n);
 const char* gemm_status_string(int status);
 
 /*
- * Device-side status: synchronises `stream`, then returns GEMM_OK or
+ * Device-side status: synchronises `stream`, then returns GEMM_OK,
  * GEMM_ERR_DEVICE_TIMEOUT if any kernel of this library on this device gave
- * up on a bounded wait since the last call (and clears the record).  The
- * kernels never trap: a wait that runs out records the fact here and the
- * kernel returns early, leaving D undefined.
+ * up on a bounded wait since the last call, or GEMM_ERR_DEVICE_CHECK if (in
+ * the checked build) a device-side bounds check failed; it clears the record.
+ * The kernels never trap: a wait that runs out, or an access a check refuses,
+ * is recorded here, the access is skipped and D is left undefined.
  */
 int gemm_device_status(gemm_handle_t h, gemm_stream_t stream);
+
+/*
+ * 1 when this library is the checked debug build (compiled with
+ * QG_DEVICE_CHECKS, libqgemm_checked.so), else 0.  In that build every work
+ * unit's tile coordinates, K range, partial slots and tile counter are checked
+ * against the problem and the workspace sizes, and every element the register
+ * epilogue reads or writes against C's / D's extent, before the access; a
+ * failed check is reported by gemm_device_status.  The checks stand in for a
+ * memory checker on machines where none can run.
+ */
+int gemm_checked_build(void);
 
 /*
  * Self-test of the device-side failure detection: launches one tiny kernel

@@ -15,6 +15,9 @@ import os
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libqgemm.so")
+# the checked debug build (device-side bounds checks); loaded instead of the
+# regular library when GEMM_DEVICE_CHECKS=1 is set in the environment
+CHECKED_LIB_PATH = os.path.join(_PKG, "libqgemm_checked.so")
 
 # ---- enums (gemm.h) -----------------------------------------------------------
 GEMM_OK = 0
@@ -25,6 +28,7 @@ GEMM_ERR_CUDA = 4
 GEMM_ERR_NO_KERNEL = 5
 GEMM_ERR_DEVICE_TIMEOUT = 6
 GEMM_ERR_BAD_CACHE = 7
+GEMM_ERR_DEVICE_CHECK = 8
 
 GEMM_F32, GEMM_F16, GEMM_BF16, GEMM_S4, GEMM_S8, GEMM_E4M3, GEMM_E5M2 = 0, 1, 2, 3, 4, 5, 6
 GEMM_ROW_MAJOR, GEMM_COL_MAJOR = 0, 1
@@ -40,7 +44,7 @@ SYMBOLS = (
     "gemm_create", "gemm_destroy", "gemm_run", "gemm_run_grouped", "gemm_export", "gemm_import",
     "gemm_get_tuning_seq", "gemm_cache_size", "gemm_status_string", "gemm_device_status",
     "gemm_selftest_wait_timeout", "gemm_last_choice", "gemm_plan_streamk", "gemm_grouped_block",
-    "gemm_run_noalloc", "gemm_heuristic_choice",
+    "gemm_run_noalloc", "gemm_heuristic_choice", "gemm_checked_build",
 )
 
 
@@ -81,10 +85,12 @@ def lib():
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH):
-        raise LibraryNotBuilt(f"{LIB_PATH} is missing; run __graft_entry__.build() or "
-                              "python quantized_gemm_tcgen05_gb300/_build.py")
-    L = ctypes.CDLL(LIB_PATH)
+    path = CHECKED_LIB_PATH if os.environ.get("GEMM_DEVICE_CHECKS") == "1" else LIB_PATH
+    if not os.path.exists(path):
+        raise LibraryNotBuilt(f"{path} is missing; run __graft_entry__.build() or "
+                              "python quantized_gemm_tcgen05_gb300/_build.py"
+                              + (" --checks" if path == CHECKED_LIB_PATH else ""))
+    L = ctypes.CDLL(path)
     P, I32, I64, SZ, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
     LP = ctypes.POINTER(gemm_layout_t)
     sig = {
@@ -108,6 +114,7 @@ def lib():
         "gemm_grouped_block": (ctypes.c_int, [ctypes.POINTER(I32), I32, I32, I64, ctypes.POINTER(I64)]),
         "gemm_heuristic_choice": (ctypes.c_int, [I64, I64, I64, I32, I32, I32, I32, I32, I32, I32, ctypes.c_size_t,
                                                  ctypes.c_char_p, ctypes.c_size_t]),
+        "gemm_checked_build": (ctypes.c_int, []),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)

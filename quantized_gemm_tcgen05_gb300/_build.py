@@ -16,6 +16,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqgemm.so")
+# the checked debug build: device-side bounds checks compiled in (QG_DEVICE_CHECKS)
+BUILD_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(PKG, "libqgemm_checked.so")
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 
@@ -51,20 +54,23 @@ def _compile(cmd, out, src, hdr_mtime, force):
     return None
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, checks: bool = False) -> str:
+    """Build libqgemm.so, or with checks=True the checked debug build
+    libqgemm_checked.so (device-side bounds checks, see gemm_checked_build)."""
+    build_dir, lib_path = (BUILD_CHECKED, LIB_CHECKED) if checks else (BUILD, LIB)
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
-    inc = ["-I", os.path.join(ROOT, "include"), "-I", CSRC]
+    inc = ["-I", os.path.join(ROOT, "include"), "-I", CSRC] + (["-DQG_DEVICE_CHECKS"] if checks else [])
     cu, cpp = sources()
     hdr = _headers_mtime()
     jobs = []
     for f in cu:
-        out = os.path.join(BUILD, f + ".o")
+        out = os.path.join(build_dir, f + ".o")
         cmd = [nvcc, "-gencode", GENCODE, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
                "-Xcompiler", "-Wall", *inc, "-c", os.path.join(CSRC, f), "-o", out]
         jobs.append((cmd, out, os.path.join(CSRC, f)))
     for f in cpp:
-        out = os.path.join(BUILD, f + ".o")
+        out = os.path.join(build_dir, f + ".o")
         cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", *inc, "-I", _cuda_include(), "-c",
                os.path.join(CSRC, f), "-o", out]
         jobs.append((cmd, out, os.path.join(CSRC, f)))
@@ -73,18 +79,20 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if errs:
         raise RuntimeError("libqgemm build failed:\n" + "\n".join(errs))
     objs = [j[1] for j in jobs]
-    if force or not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or not os.path.exists(lib_path) or any(os.path.getmtime(o) > os.path.getmtime(lib_path) for o in objs):
+        tmp = lib_path + f".tmp{os.getpid()}"
         cmd = [nvcc, "-shared", "-gencode", GENCODE, "-Xcompiler", "-fPIC", "-o", tmp, *objs,
                "-cudart", "static", "-lpthread", "-ldl", "-lrt"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"libqgemm link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib_path)
     if verbose:
-        print("built", LIB)
-    return LIB
+        print("built", lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    build(verbose=True)
+    import sys
+
+    build(verbose=True, checks="--checks" in sys.argv[1:])

@@ -24,6 +24,12 @@
 
 using namespace qg;
 
+#ifdef QG_DEVICE_CHECKS
+static constexpr bool kDeviceChecksHost = true;
+#else
+static constexpr bool kDeviceChecksHost = false;
+#endif
+
 struct gemm_handle {
     int device = 0;
     int sm_count = 0;
@@ -134,6 +140,27 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int qg::handle_device(gemm_handle_t h) { return h ? h->device : -1; }
 
+namespace {
+
+// Elements of D (or C) a call may touch: batches x rows, the last row N long.
+int64_t out_extent(int64_t M, int64_t N, int64_t ld, int32_t batches, int64_t bstride) {
+    if (M <= 0 || N <= 0) return 0;
+    return (int64_t)(batches > 1 ? batches - 1 : 0) * bstride + (M - 1) * ld + N;
+}
+
+// The checked build's self-test knob: GEMM_CHECK_SHRINK_WORKSPACE=1 tells the
+// kernels a quarter of the partials buffer the caller passed (the buffer
+// itself is whole, so the accesses the check then skips stay inside it).
+uint64_t checked_partials_bytes(uint64_t bytes) {
+#ifdef QG_DEVICE_CHECKS
+    const char* e = getenv("GEMM_CHECK_SHRINK_WORKSPACE");
+    if (e && e[0] == '1') return bytes / 4;
+#endif
+    return bytes;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* gemm_status_string(int s) {
@@ -146,6 +173,7 @@ const char* gemm_status_string(int s) {
         case GEMM_ERR_NO_KERNEL: return "no kernel accepts the problem";
         case GEMM_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded wait";
         case GEMM_ERR_BAD_CACHE: return "malformed or foreign dispatch cache";
+        case GEMM_ERR_DEVICE_CHECK: return "a device-side bounds check failed (checked build)";
         default: return "unknown status";
     }
 }
@@ -398,6 +426,8 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
         if (!aligned16(ws->partials) || (reinterpret_cast<uintptr_t>(ws->barriers) & 3u)) return GEMM_ERR_INVALID_ARG;
         kp.partials = static_cast<float*>(ws->partials);
         kp.counters = static_cast<int32_t*>(ws->barriers);
+        kp.partials_bytes = checked_partials_bytes(ws->partials_size);
+        kp.counters_bytes = ws->barriers_size;
     }
     EpiParams& e = kp.epi;
     e.D = p.D;
@@ -406,6 +436,9 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
     e.ldc = p.ldc;
     e.d_bstride = is_grouped(p) ? 0 : p.d_bs;
     e.c_bstride = is_grouped(p) ? 0 : p.c_bs;
+    e.d_extent = out_extent(p.M, p.N, p.ldd, is_grouped(p) ? 1 : p.batches, p.d_bs);
+    e.c_extent = e.C ? out_extent(p.M, p.N, p.ldc, is_grouped(p) ? 1 : p.batches, p.c_bs) : 0;
+    e.status = h->status;
     e.M = p.M;
     e.N = p.N;
     e.alpha = p.alpha;
@@ -702,6 +735,9 @@ int dispatch_and_run(gemm_handle* h, const gemm_op_t* op, Problem& p, const gemm
         e.bias_type = p.bias_type;
         e.qscale = p.qscale;
         e.qzp = p.qzp;
+        e.d_extent = out_extent(p.M, p.N, p.ldd, p.batches, p.d_bs);
+        e.c_extent = e.C ? out_extent(p.M, p.N, p.ldc, p.batches, p.c_bs) : 0;
+        e.status = h->status;
         h->last_choice = "scale_c";
         return launch_scale_c(e, p.batches, st) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
@@ -1016,6 +1052,8 @@ int gemm_cache_size(gemm_handle_t h, int32_t* n) {
     return GEMM_OK;
 }
 
+int gemm_checked_build(void) { return kDeviceChecksHost ? 1 : 0; }
+
 int gemm_device_status(gemm_handle_t h, gemm_stream_t stream) {
     if (!h) return GEMM_ERR_INVALID_ARG;
     int rc = bind_device(h);
@@ -1031,12 +1069,13 @@ int gemm_device_status(gemm_handle_t h, gemm_stream_t stream) {
     }
     if (st[0] == 0) return GEMM_OK;
     if (h->log)
-        fprintf(stderr, "qgemm: device wait gave up (site %u, block %u, count %u)\n", st[1], st[2], st[3]);
+        fprintf(stderr, "qgemm: device %s (site %u, block %u, count %u)\n",
+                (st[0] & 2u) ? "bounds check failed" : "wait gave up", st[1], st[2], st[3]);
     if (cudaMemset(h->status, 0, sizeof st) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
-    return GEMM_ERR_DEVICE_TIMEOUT;
+    return (st[0] & 2u) ? GEMM_ERR_DEVICE_CHECK : GEMM_ERR_DEVICE_TIMEOUT;
 }
 
 int gemm_selftest_wait_timeout(gemm_handle_t h, uint64_t timeout_ns, gemm_stream_t stream) {

@@ -113,6 +113,30 @@ __device__ __forceinline__ bool wait_bar_drain(uint64_t* bar, uint32_t parity, c
 
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// ---- device-side bounds checks (debug build) ------------------------------------
+//
+// Built with QG_DEVICE_CHECKS (the checked library, GEMM_DEVICE_CHECKS=1 at
+// build time), every unit's tile coordinates, K range, partial slots and tile
+// counter are checked against the problem and the workspace the host passed,
+// and every element the register epilogue reads or writes against C's / D's
+// extent.  A failed check records its site in the device status words (bit 1
+// of the first word) and the access is skipped, so the kernel never touches
+// memory outside its operands; gemm_device_status then reports it.  The
+// regular build compiles none of this.
+#ifdef QG_DEVICE_CHECKS
+constexpr bool kDeviceChecks = true;
+#else
+constexpr bool kDeviceChecks = false;
+#endif
+
+static __device__ __noinline__ void record_check(uint32_t* status, uint32_t site) {
+    if (!status) return;
+    atomicExch(&status[1], site);
+    atomicExch(&status[2], blockIdx.x);
+    atomicAdd(&status[3], 1u);
+    atomicOr(&status[0], 2u);
+}
+
 // ---- unit iteration shared by all roles ----------------------------------------
 //
 // A 1-CTA kernel walks 128-row tiles with program id blockIdx.x.  The CTA-pair
@@ -123,15 +147,23 @@ __device__ __forceinline__ int unit_pid(const GemmKernelParams& P) {
     return P.pair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
 }
 
+static __device__ bool unit_in_bounds(const GemmKernelParams& P, const Unit& u, int bn);
+
 __device__ __forceinline__ bool next_unit(const GemmKernelParams& P, WorkIter& w, Unit& u, int bn) {
-    if (!P.pair) return w.next(P.sched, (int)blockIdx.x, BM, bn, u);
-    if (!w.next(P.sched, (int)(blockIdx.x >> 1), 2 * BM, bn, u)) return false;
-    const int32_t half = (int32_t)(blockIdx.x & 1);
-    u.x_row0 += (int64_t)half * BM;
-    // a grouped 256-row block may hold fewer rows of its expert: each CTA
-    // keeps its share (possibly none; the epilogue then stores nothing)
-    const int32_t rows = P.sched.grouped ? u.x_rows - half * BM : BM;
-    u.x_rows = rows < 0 ? 0 : (rows > BM ? BM : rows);
+    if (!P.pair) {
+        if (!w.next(P.sched, (int)blockIdx.x, BM, bn, u)) return false;
+    } else {
+        if (!w.next(P.sched, (int)(blockIdx.x >> 1), 2 * BM, bn, u)) return false;
+        const int32_t half = (int32_t)(blockIdx.x & 1);
+        u.x_row0 += (int64_t)half * BM;
+        // a grouped 256-row block may hold fewer rows of its expert: each CTA
+        // keeps its share (possibly none; the epilogue then stores nothing)
+        const int32_t rows = P.sched.grouped ? u.x_rows - half * BM : BM;
+        u.x_rows = rows < 0 ? 0 : (rows > BM ? BM : rows);
+    }
+    if constexpr (kDeviceChecks) {
+        if (!unit_in_bounds(P, u, bn)) return false;  // recorded; this role stops
+    }
     return true;
 }
 
@@ -205,8 +237,21 @@ __device__ __forceinline__ float bias_at(const EpiParams& e, int64_t n) {
 // Store one output value of row m at element index i: rounded to D's type, or
 // (Q8) quantised with the row's scale for an int8 D.  Callers choose Q8 once
 // per chunk, so the float store carries no extra per-element test.
+// Checked build: element index i (and the three after it for a vector access)
+// inside extent; records and returns false otherwise.
+__device__ __forceinline__ bool elem_in_bounds(const EpiParams& e, int64_t i, int64_t n, int64_t extent) {
+    if constexpr (kDeviceChecks) {
+        if (i < 0 || i + n > extent) {
+            record_check(e.status, CHECK_ELEMENT);
+            return false;
+        }
+    }
+    return true;
+}
+
 template <bool Q8 = true>
 __device__ __forceinline__ void store_out(const EpiParams& e, int64_t i, float x, int64_t m) {
+    if (!elem_in_bounds(e, i, 1, e.d_extent)) return;
     if (Q8 && e.d_type == DT_S8)
         static_cast<int8_t*>(e.D)[i] = (int8_t)quant_s8(x, e.qscale[m], e.qzp);
     else
@@ -216,6 +261,7 @@ __device__ __forceinline__ void store_out(const EpiParams& e, int64_t i, float x
 // Four consecutive values of row m (aligned as st4 needs; 4 bytes for int8).
 template <bool Q8 = true>
 __device__ __forceinline__ void store_out4(const EpiParams& e, int64_t i, float4 v, int64_t m) {
+    if (!elem_in_bounds(e, i, 4, e.d_extent)) return;
     if (Q8 && e.d_type == DT_S8) {
         const float s = e.qscale[m];
         const uint32_t b = (uint32_t)(quant_s8(v.x, s, e.qzp) & 0xFF) | ((uint32_t)(quant_s8(v.y, s, e.qzp) & 0xFF) << 8) |
@@ -332,7 +378,9 @@ __device__ __forceinline__ void load_c_chunk(const EpiParams& e, const Unit& u, 
 #pragma unroll
         for (int j = 0; j < W; ++j) {
             const int64_t m = u.y_row0 + col0 + j;
-            cc.v[j] = (nok && m < e.M) ? ld_elem(e.C, e.d_type, boff_c + m * e.ldc + n) : 0.0f;
+            cc.v[j] = (nok && m < e.M && elem_in_bounds(e, boff_c + m * e.ldc + n, 1, e.c_extent))
+                          ? ld_elem(e.C, e.d_type, boff_c + m * e.ldc + n)
+                          : 0.0f;
         }
         return;
     }
@@ -345,7 +393,8 @@ __device__ __forceinline__ void load_c_chunk(const EpiParams& e, const Unit& u, 
         const int64_t m = u.x_row0 + rt;
         const int64_t n0 = u.y_row0 + col0 + 4 * j;
         float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (rt < u.x_rows && m < e.M && n0 < e.N) {
+        if (rt < u.x_rows && m < e.M && n0 < e.N &&
+            elem_in_bounds(e, boff_c + m * e.ldc + n0, e.N - n0 < 4 ? e.N - n0 : 4, e.c_extent)) {
             const int64_t ci = boff_c + m * e.ldc + n0;
             if (e.vec_ok && n0 + 3 < e.N) {
                 c = ld4(e.C, e.d_type, ci);
@@ -454,6 +503,43 @@ __device__ __forceinline__ int64_t half_slot(const GemmKernelParams& P, int64_t 
 }
 __device__ __forceinline__ int32_t* tile_counter(const GemmKernelParams& P, int64_t tile) {
     return &P.counters[P.pair ? 2 * tile + (blockIdx.x & 1) : tile];
+}
+
+// The checked build's unit check: tile coordinates inside the tile grid (or,
+// grouped, the expert and its token rows inside the problem), a K range inside
+// the K-steps, and for a split tile every contributor's partial slot and the
+// tile's counter inside the workspace.
+static __device__ __noinline__ bool unit_in_bounds(const GemmKernelParams& P, const Unit& u, int bn) {
+    const SchedParams& s = P.sched;
+    const int64_t rows_x = (int64_t)s.tiles_x * BM * (P.pair ? 2 : 1), rows_y = (int64_t)s.tiles_y * bn;
+    bool ok = u.k_begin >= 0 && u.k_begin < u.k_end && u.k_end <= s.k_iters && u.tile >= 0 && u.tile < total_tiles(s) &&
+              u.y_row0 >= 0 && u.y_row0 < rows_y && u.x_rows >= 0 && u.x_rows <= BM;
+    if (s.grouped)  // a CTA-pair half with no rows of its expert stores nothing (its copies read zeros)
+        ok = ok && u.batch >= 0 && u.batch < s.num_experts && u.x_row0 >= 0 &&
+             (u.x_rows == 0 || u.x_row0 + u.x_rows <= (int64_t)s.expert_offsets[s.num_experts]);
+    else
+        ok = ok && u.batch >= 0 && u.batch < s.batches && u.x_row0 >= 0 && u.x_row0 < rows_x;
+    if (!ok) {
+        record_check(P.status, CHECK_UNIT);
+        return false;
+    }
+    if (u.mode == UNIT_PARTIAL) {
+        // both halves of a CTA pair are checked, so the two CTAs always agree
+        const uint64_t slot_bytes = (uint64_t)BM * bn * 4;
+        const int64_t halves = P.pair ? 2 : 1;
+        for (int q = 0; q <= u.ncontrib; ++q) {
+            const int64_t sl = q < u.ncontrib ? partial_slot(s, u.tile, q) : u.slot;
+            if (sl < 0 || (uint64_t)(halves * sl + halves) * slot_bytes > P.partials_bytes) {
+                record_check(P.status, CHECK_PARTIAL);
+                return false;
+            }
+        }
+        if ((uint64_t)(halves * u.tile + halves) * 4 > P.counters_bytes) {
+            record_check(P.status, CHECK_COUNTER);
+            return false;
+        }
+    }
+    return true;
 }
 
 // Whether unit `u` (just returned by the iterator `w`) is this program's last.

@@ -25,6 +25,16 @@ enum WaitSite : uint32_t {
     SITE_SELFTEST = 9,
 };
 
+// Where a device-side bounds check failed (checked builds only, see
+// QG_DEVICE_CHECKS in common.cuh): recorded in the same status words, with
+// bit 1 of the first word set.
+enum CheckSite : uint32_t {
+    CHECK_UNIT = 16,     // a unit's tile coordinates or K range outside the problem
+    CHECK_PARTIAL = 17,  // a partial slot outside the workspace's partials
+    CHECK_COUNTER = 18,  // a tile counter outside the workspace's barriers
+    CHECK_ELEMENT = 19,  // an element of C or D outside its extent
+};
+
 // Epilogue: D = fma(alpha, acc, beta * C) rounded to D's type.
 struct EpiParams {
     void* D;
@@ -43,6 +53,8 @@ struct EpiParams {
     const void* bias;  // N values, one per output column (EPI_BIAS)
     const float* qscale;  // d_type DT_S8: M scales, one per output row
     int32_t qzp;          // d_type DT_S8: zero point
+    int64_t d_extent, c_extent;  // elements of D / C the call may touch (bounds of the checked build)
+    uint32_t* status;            // device status words (the checked build records failed checks there)
 };
 
 // Fused epilogue steps after x = alpha * acc + beta * c: + bias[column], then
@@ -86,6 +98,8 @@ struct GemmKernelParams {
     int32_t ks;           // K-steps per stage (>1: X/Y maps index K chunks of one K-step)
     int32_t kstep;        // elements per K-step: one 128-byte swizzle row (64 16-bit, 128 8-bit values)
     int32_t mma_f8;       // operands are 8-bit floats: tcgen05.mma.kind::f8f6f4
+    uint64_t partials_bytes;  // workspace sizes (bounds of the checked build)
+    uint64_t counters_bytes;
 };
 
 // Instruction descriptor of tcgen05.mma.kind::f16: fp32 accumulator (bits

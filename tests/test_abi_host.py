@@ -152,3 +152,24 @@ def test_small_m_kernel_limits(monkeypatch):
     monkeypatch.setenv("GEMM_GEMV_MAX_M", "8")
     assert qg.gemm_heuristic_choice(8, 4096, 4096, bf, bf, bf) == "gemv"
     assert qg.gemm_heuristic_choice(9, 4096, 4096, bf, bf, bf) != "gemv"
+
+
+def test_checked_build_compiles(tmp_path):
+    """The device-side bounds checks (QG_DEVICE_CHECKS) compile for sm_103a
+    (one kernel instantiation; the checks live in the code every kernel
+    shares), and the regular library reports that it is not the checked
+    build."""
+    import shutil
+    import subprocess
+
+    from quantized_gemm_tcgen05_gb300 import _build
+
+    if shutil.which(_build._nvcc()) is None and not os.path.exists(_build._nvcc()):
+        pytest.skip("no nvcc")
+    for src in ("umma_gemm_bn16.cu",):  # the checks live in the shared epilogue / unit code
+        cmd = [_build._nvcc(), "-gencode", _build.GENCODE, "-O1", "-std=c++17", "-DQG_DEVICE_CHECKS", "-I",
+               os.path.join(ROOT, "include"), "-I", _build.CSRC, "-c", os.path.join(_build.CSRC, src), "-o",
+               str(tmp_path / (src + ".o"))]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr[-2000:]
+    assert qg.lib().gemm_checked_build() == 0
