@@ -129,11 +129,6 @@ template <int MT, int U, bool BF16, bool INT4>
 __global__ void __launch_bounds__(GEMV_WARPS * 32, MT == 1 ? 4 : 2) gemv_kernel(const GemvParams p, uint64_t gmagic) {
     constexpr int R = GEMV_R;
     __shared__ float red[GEMV_WARPS][MT][R];
-    // every CTA of the grid is resident (one wave), so the next kernel may
-    // start its set-up now; it waits for this grid before touching memory
-    griddep_launch_dependents();
-    griddep_wait();
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.kslices;
     const int groups_per_cta = GEMV_WARPS / S;
@@ -145,6 +140,28 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, MT == 1 ? 4 : 2) gemv_kernel(
     const int64_t cend = cbeg + cps < nchunk ? cbeg + cps : nchunk;
     const int64_t row_bytes = INT4 ? p.ldb / 2 : p.ldb * 2;
     const int64_t ngroups = (p.N + R - 1) / R;
+    // every CTA of the grid is resident (one wave), so the next kernel may
+    // start its set-up now; it waits for this grid before touching memory
+    griddep_launch_dependents();
+    // meanwhile warm L2 with this warp's first weight chunks (a hint only: L2
+    // is where memory is coherent, so a write by the previous kernel still
+    // reaches the loads below)
+    {
+        const int64_t grp = (int64_t)blockIdx.x * groups_per_cta + gi;
+        if (grp < ngroups) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int64_t row = grp * R + r < p.N ? grp * R + r : p.N - 1;
+                const uint8_t* base = reinterpret_cast<const uint8_t*>(p.B) + row * row_bytes;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t c = cbeg + lane + 32 * u;
+                    if (c < cend) asm volatile("prefetch.global.L2 [%0];" ::"l"(base + c * 16));
+                }
+            }
+        }
+    }
+    griddep_wait();
     const uint16_t* A = reinterpret_cast<const uint16_t*>(p.A);
     const bool scaled = p.V != nullptr;
 

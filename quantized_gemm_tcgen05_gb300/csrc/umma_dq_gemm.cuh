@@ -339,6 +339,21 @@ __global__ void __launch_bounds__(192 + XF_THREADS, 1)
         if (P.dq.x.has_scale) tma_prefetch_desc(&tmXs);
         if (P.dq.y.has_scale) tma_prefetch_desc(&tmYs);
         if (P.dq.x.has_zero || P.dq.y.has_zero) tma_prefetch_desc(&tmZ);
+        // warm L2 with the first stages' operands while the previous kernel in
+        // the stream finishes (not for grouped problems: their tile map reads
+        // memory the previous kernel may write)
+        if (!P.sched.grouped) {
+            WorkIter w;
+            w.init(P.sched, blockIdx.x);
+            Unit u;
+            if (w.next(P.sched, blockIdx.x, BM, BN, u)) {
+                const int kend = u.k_end < u.k_begin + S ? u.k_end : u.k_begin + S;
+                for (int k = u.k_begin; k < kend; ++k) {
+                    tma_prefetch_l2_2d(&tmX, P.dq.x.int4 ? k * (BK / 2) : k * BK, (int32_t)u.x_row0);
+                    tma_prefetch_l2_2d(&tmY, P.dq.y.int4 ? k * (BK / 2) : k * BK, (int32_t)u.y_row0);
+                }
+            }
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, Cfg::TMEM_COLS);

@@ -93,6 +93,32 @@ __global__ void __launch_bounds__(192, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmX);
         tma_prefetch_desc(&tmY);
+        // warm L2 with the first stages' operands while the previous kernel in
+        // the stream finishes (grouped problems read their tile map from memory
+        // the previous kernel may write, so they wait)
+        if (!P.sched.grouped) {
+            WorkIter w;
+            w.init(P.sched, blockIdx.x);
+            Unit u;
+            if (w.next(P.sched, blockIdx.x, BM, BN, u)) {
+                const int kend = u.k_end < u.k_begin + S * KS ? u.k_end : u.k_begin + S * KS;
+                for (int k = u.k_begin; k < kend; k += KS) {
+                    if (KS > 1) {
+                        tma_prefetch_l2_3d(&tmX, 0, (int32_t)u.x_row0, k);
+                        tma_prefetch_l2_3d(&tmY, 0, (int32_t)u.y_row0, k);
+                    } else {
+                        if (P.x3d)
+                            tma_prefetch_l2_3d(&tmX, k * P.kstep, (int32_t)u.x_row0, u.batch);
+                        else
+                            tma_prefetch_l2_2d(&tmX, k * P.kstep, (int32_t)u.x_row0);
+                        if (P.y3d)
+                            tma_prefetch_l2_3d(&tmY, k * P.kstep, (int32_t)u.y_row0, u.batch);
+                        else
+                            tma_prefetch_l2_2d(&tmY, k * P.kstep, (int32_t)u.y_row0);
+                    }
+                }
+            }
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
@@ -169,35 +195,42 @@ __global__ void __launch_bounds__(192, 1)
                 if (!wait_bar(&tempty[buf], aph ^ 1, g, SITE_MMA_TMEM_EMPTY)) break;
                 tc_fence_after_sync();
                 const uint32_t d = tmem_base + (uint32_t)(buf * BN);
-                for (int k = u.k_begin; k < u.k_end; k += KS) {
-                    if (!wait_bar(&full[s], ph, g, SITE_MMA_FULL)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint32_t a_addr = smem_u32(ring + (size_t)s * stage_bytes);
-                    const int nk = u.k_end - k < KS ? u.k_end - k : KS;
-                    for (int h = 0; h < nk; ++h) {
-                        const uint64_t ad = make_sw128_kmajor_desc(a_addr + h * Cfg::A_BYTES);
-                        const uint64_t bd = make_sw128_kmajor_desc(a_addr + a_region + h * Cfg::B_BYTES);
-                        // four instructions per K-step, 32 bytes of each operand row apiece
-                        if (P.mma_f8) {
+                // the K loop of one unit, for one MMA kind (chosen once per
+                // launch, outside the loop): four instructions per K-step, 32
+                // bytes of each operand row apiece
+                auto k_loop = [&](auto f8) {
+                    for (int k = u.k_begin; k < u.k_end; k += KS) {
+                        if (!wait_bar(&full[s], ph, g, SITE_MMA_FULL)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const uint32_t a_addr = smem_u32(ring + (size_t)s * stage_bytes);
+                        const int nk = u.k_end - k < KS ? u.k_end - k : KS;
+                        for (int h = 0; h < nk; ++h) {
+                            const uint64_t ad = make_sw128_kmajor_desc(a_addr + h * Cfg::A_BYTES);
+                            const uint64_t bd = make_sw128_kmajor_desc(a_addr + a_region + h * Cfg::B_BYTES);
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                umma_f8_ss(d, ad + 2 * kk, bd + 2 * kk, P.idesc, (k + h > u.k_begin || kk > 0) ? 1u : 0u);
-                        } else {
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                umma_f16_ss(d, ad + 2 * kk, bd + 2 * kk, P.idesc, (k + h > u.k_begin || kk > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint32_t acc = (k + h > u.k_begin || kk > 0) ? 1u : 0u;
+                                if constexpr (decltype(f8)::value)
+                                    umma_f8_ss(d, ad + 2 * kk, bd + 2 * kk, P.idesc, acc);
+                                else
+                                    umma_f16_ss(d, ad + 2 * kk, bd + 2 * kk, P.idesc, acc);
+                            }
+                        }
+                        issued = true;
+                        umma_commit(&empty[s]);
+                        if (++s == S) {
+                            s = 0;
+                            ph ^= 1;
                         }
                     }
-                    issued = true;
-                    umma_commit(&empty[s]);
-                    if (++s == S) {
-                        s = 0;
-                        ph ^= 1;
-                    }
-                }
+                };
+                if (P.mma_f8)
+                    k_loop(std::true_type{});
+                else
+                    k_loop(std::false_type{});
                 if (!ok) break;
                 umma_commit(&tfull[buf]);
             }

@@ -227,37 +227,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     break;
                 tc_fence_after_sync();
                 const uint32_t d = tmem_base + (uint32_t)(buf * BN);
-                for (int k = u.k_begin; k < u.k_end; k += KS) {
-                    if (!wait_bar(&full[s], ph, g, SITE_MMA_FULL)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint32_t a_addr = smem_u32(ring + (size_t)s * stage_bytes);
-                    const int nk = u.k_end - k < KS ? u.k_end - k : KS;
-                    for (int h = 0; h < nk; ++h) {
-                        const uint64_t ad = make_sw128_kmajor_desc(a_addr + h * Cfg::A_BYTES);
-                        const uint64_t bd = make_sw128_kmajor_desc(a_addr + a_region + h * Cfg::B_BYTES);
-                        // four instructions per K-step, 32 bytes of each operand row apiece
-                        if (P.mma_f8) {
+                // the K loop of one unit, for one MMA kind (chosen once per
+                // launch, outside the loop): four instructions per K-step, 32
+                // bytes of each operand row apiece
+                auto k_loop = [&](auto f8) {
+                    for (int k = u.k_begin; k < u.k_end; k += KS) {
+                        if (!wait_bar(&full[s], ph, g, SITE_MMA_FULL)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const uint32_t a_addr = smem_u32(ring + (size_t)s * stage_bytes);
+                        const int nk = u.k_end - k < KS ? u.k_end - k : KS;
+                        for (int h = 0; h < nk; ++h) {
+                            const uint64_t ad = make_sw128_kmajor_desc(a_addr + h * Cfg::A_BYTES);
+                            const uint64_t bd = make_sw128_kmajor_desc(a_addr + a_region + h * Cfg::B_BYTES);
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                umma_f8_ss_pair(d, ad + 2 * kk, bd + 2 * kk, P.idesc,
-                                                (k + h > u.k_begin || kk > 0) ? 1u : 0u);
-                        } else {
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                umma_f16_ss_pair(d, ad + 2 * kk, bd + 2 * kk, P.idesc,
-                                                 (k + h > u.k_begin || kk > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint32_t acc = (k + h > u.k_begin || kk > 0) ? 1u : 0u;
+                                if constexpr (decltype(f8)::value)
+                                    umma_f8_ss_pair(d, ad + 2 * kk, bd + 2 * kk, P.idesc, acc);
+                                else
+                                    umma_f16_ss_pair(d, ad + 2 * kk, bd + 2 * kk, P.idesc, acc);
+                            }
+                        }
+                        issued = true;
+                        umma_commit_pair_mc(&empty[s], 0x3);
+                        if (++s == S) {
+                            s = 0;
+                            ph ^= 1;
                         }
                     }
-                    issued = true;
-                    umma_commit_pair_mc(&empty[s], 0x3);
-                    if (++s == S) {
-                        s = 0;
-                        ph ^= 1;
-                    }
-                }
+                };
+                if (P.mma_f8)
+                    k_loop(std::true_type{});
+                else
+                    k_loop(std::false_type{});
                 if (!ok) break;
                 umma_commit_pair_mc(&tfull[buf], 0x3);
             }
