@@ -209,6 +209,34 @@ __device__ __forceinline__ float4 ld4(const void* p, int32_t t, int64_t i) {
     return r;
 }
 
+// Eight consecutive 16-bit elements (F16 or BF16), 16-byte aligned.
+__device__ __forceinline__ void ld8(const void* p, int32_t t, int64_t i, float (&o)[8]) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p) + i);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f = t == DT_F16 ? __half22float2(*reinterpret_cast<const __half2*>(&w[q]))
+                                     : __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
+        o[2 * q] = f.x;
+        o[2 * q + 1] = f.y;
+    }
+}
+
+__device__ __forceinline__ void st8(void* p, int32_t t, int64_t i, const float (&v)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (t == DT_F16) {
+            const __half2 h = __floats2half2_rn(v[2 * q], v[2 * q + 1]);
+            w[q] = *reinterpret_cast<const uint32_t*>(&h);
+        } else {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+            w[q] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+    }
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p) + i) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 __device__ __forceinline__ void st4(void* p, int32_t t, int64_t i, float4 v) {
     if (t == DT_F32) {
         *reinterpret_cast<float4*>(static_cast<float*>(p) + i) = v;
@@ -289,6 +317,38 @@ __device__ __forceinline__ void prefetch_bias(const EpiParams& e, int64_t first,
     }
 }
 
+// Bring the C block a unit combines into L2 before its accumulator is ready,
+// so the register epilogue's per-chunk C loads do not each wait on HBM.  This
+// warp's share: its 32 tile rows (output rows, or output columns when the
+// operands are swapped) across the tile's bn columns; one prefetch per
+// 128-byte line, spread over the lanes.
+__device__ __forceinline__ void prefetch_c_l2(const EpiParams& e, const Unit& u, int ew, int lane, int bn) {
+    if (e.beta == 0.0f || e.C == nullptr) return;
+    const int64_t es = e.d_type == DT_F32 ? 4 : 2;
+    const char* base = static_cast<const char*>(e.C) + (int64_t)u.batch * e.c_bstride * es;
+    if (!e.swap) {
+        // rows x_row0 + ew*32 .. +31, columns y_row0 .. +bn
+        const int64_t row_bytes = (e.N - u.y_row0 < bn ? e.N - u.y_row0 : bn) * es;
+        const int lines = (int)((row_bytes + 127) / 128);
+        for (int i = lane; i < 32 * lines; i += 32) {
+            const int rt = ew * 32 + i / lines;
+            const int64_t m = u.x_row0 + rt;
+            if (rt >= u.x_rows || m >= e.M) continue;
+            const char* a = base + (m * e.ldc + u.y_row0) * es + (int64_t)(i % lines) * 128;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+        }
+    } else {
+        // output rows y_row0 .. +bn, columns x_row0 + ew*32 .. +31
+        const int64_t n0 = u.x_row0 + ew * 32;
+        if (n0 >= e.N || ew * 32 >= u.x_rows) return;
+        for (int j = lane; j < bn; j += 32) {
+            const int64_t m = u.y_row0 + j;
+            if (m >= e.M) break;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(base + (m * e.ldc + n0) * es));
+        }
+    }
+}
+
 // The fused steps after x = alpha * acc + beta * c: + bias, then ReLU (keeps
 // NaN) or GELU in the exact form x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)).
 __device__ __forceinline__ float epi_finish(const EpiParams& e, float x, float bias) {
@@ -364,12 +424,43 @@ struct CChunk {
     float v[W];
 };
 
+// Whether a non-swapped chunk moves through global memory in 8-column
+// pieces (16 bytes of a 16-bit C / D per lane) rather than 4-column ones.
+__device__ __forceinline__ bool octet_layout(const EpiParams& e) {
+    return e.vec_ok && (e.d_type == DT_F16 || e.d_type == DT_BF16);
+}
+
 // Row-per-thread layout (non-swapped): iteration `it` of a thread covers tile
-// row ew*32 + it*(32/Q) + lane/Q and the 4 columns 4*(lane%Q) .. +3.
+// row ew*32 + it*(32/Q) + lane/Q and the 4 columns 4*(lane%Q) .. +3; in the
+// octet layout, tile row ew*32 + it*(32/O) + lane/O and the 8 columns
+// 8*(lane%O) .. +7 (O = W/8 pieces per row).
 template <int W>
 __device__ __forceinline__ void load_c_chunk(const EpiParams& e, const Unit& u, int ew, int lane, int col0,
                                              CChunk<W>& cc) {
     if (e.beta == 0.0f) return;
+    if (!e.swap && octet_layout(e)) {
+        constexpr int O = W / 8, ROWS = 32 / O;
+        const int64_t boff = (int64_t)u.batch * e.c_bstride;
+#pragma unroll
+        for (int it = 0; it < O; ++it) {
+            const int rt = ew * 32 + it * ROWS + lane / O;
+            const int64_t m = u.x_row0 + rt;
+            const int64_t n0 = u.y_row0 + col0 + 8 * (lane % O);
+            float c[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const int64_t ci = boff + m * e.ldc + n0;
+            if (rt < u.x_rows && m < e.M && n0 < e.N &&
+                elem_in_bounds(e, ci, e.N - n0 < 8 ? e.N - n0 : 8, e.c_extent)) {
+                if (n0 + 7 < e.N) {
+                    ld8(e.C, e.d_type, ci, c);
+                } else {
+                    for (int t = 0; t < 8 && n0 + t < e.N; ++t) c[t] = ld_elem(e.C, e.d_type, ci + t);
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < 8; ++t) cc.v[8 * it + t] = c[t];
+        }
+        return;
+    }
     constexpr int Q = W / 4;
     const int64_t boff_c = (int64_t)u.batch * e.c_bstride;
     if (e.swap) {
@@ -422,9 +513,37 @@ __device__ __forceinline__ void store_chunk_t(const EpiParams& e, const Unit& u,
     constexpr int Q = W / 4;
     const int64_t boff_d = (int64_t)u.batch * e.d_bstride;
     if (e.swap) {
-        // tile row -> output column n; tile column -> output row m.  Lanes
-        // hold consecutive n, so each store instruction is row-contiguous.
-        const int64_t n = u.x_row0 + ew * 32 + lane;
+        // tile row -> output column n; tile column -> output row m.
+        const int64_t nb = u.x_row0 + ew * 32;  // this warp's 32 output columns
+        if (!Q8 && e.d_type != DT_F32 && e.vec_ok && nb + 32 <= e.N && ew * 32 + 32 <= u.x_rows) {
+            // 16-bit D, whole warp in range: through the staging buffer, so
+            // that every lane stores 16 bytes (a quarter of one output row's
+            // 32 columns) instead of one element per chunk column
+            constexpr int PITCH = 40;  // halves per staged row: 80 bytes keeps the 16-byte reads spread over the banks
+            uint16_t* t16 = reinterpret_cast<uint16_t*>(staging);
+            const float bn = ACT >= 0 ? bias_at(e, nb + lane) : 0.0f;
+#pragma unroll
+            for (int j = 0; j < W; ++j) {
+                const float x = epi_value<ACT>(e, v[j], cc.v[j], bn);
+                t16[j * PITCH + lane] = e.d_type == DT_F16 ? __half_as_ushort(__float2half_rn(x))
+                                                           : __bfloat16_as_ushort(__float2bfloat16_rn(x));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int it = 0; it < W / 8; ++it) {
+                const int j = it * 8 + lane / 4, part = lane % 4;
+                const int64_t m = u.y_row0 + col0 + j;
+                const int64_t di = boff_d + m * e.ldd + nb + part * 8;
+                const uint4 q = *reinterpret_cast<const uint4*>(t16 + j * PITCH + part * 8);
+                if (m < e.M && elem_in_bounds(e, di, 8, e.d_extent))
+                    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(e.D) + di) = q;
+            }
+            __syncwarp();
+            return;
+        }
+        // otherwise one element per store; lanes hold consecutive n, so each
+        // store instruction is still row-contiguous
+        const int64_t n = nb + lane;
         if (n >= e.N || ew * 32 + lane >= u.x_rows) return;
         const float bn = ACT >= 0 ? bias_at(e, n) : 0.0f;
 #pragma unroll
@@ -438,6 +557,34 @@ __device__ __forceinline__ void store_chunk_t(const EpiParams& e, const Unit& u,
     for (int j = 0; j < Q; ++j)
         staging[lane * Q + (j ^ (lane & (Q - 1)))] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     __syncwarp();
+    if (!Q8 && octet_layout(e)) {
+        // 16-bit D: two staged quads per lane, one 16-byte store
+        constexpr int O = W / 8, ROWS = 32 / O;
+        const int o = lane % O;
+#pragma unroll
+        for (int it = 0; it < O; ++it) {
+            const int rr = it * ROWS + lane / O;
+            const float4 a = staging[rr * Q + ((2 * o) ^ (rr & (Q - 1)))];
+            const float4 b = staging[rr * Q + ((2 * o + 1) ^ (rr & (Q - 1)))];
+            const int rt = ew * 32 + rr;
+            const int64_t m = u.x_row0 + rt;
+            const int64_t n0 = u.y_row0 + col0 + 8 * o;
+            if (rt >= u.x_rows || m >= e.M || n0 >= e.N) continue;
+            const float acc[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            float out[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+                out[t] = epi_value<ACT>(e, acc[t], cc.v[8 * it + t], ACT >= 0 ? bias_at(e, n0 + t) : 0.0f);
+            const int64_t di = boff_d + m * e.ldd + n0;
+            if (n0 + 7 < e.N) {
+                if (elem_in_bounds(e, di, 8, e.d_extent)) st8(e.D, e.d_type, di, out);
+            } else {
+                for (int t = 0; t < 8 && n0 + t < e.N; ++t) store_out<false>(e, di + t, out[t], m);
+            }
+        }
+        __syncwarp();
+        return;
+    }
     constexpr int ROWS_PER_IT = 32 / Q;
     // this lane's quad of columns is the same in every iteration
     float bq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -658,6 +805,7 @@ __device__ void epilogue_role(const GemmKernelParams& P, uint32_t tmem_base, uin
             else
                 prefetch_bias(P.epi, u.y_row0, BN, lane);
         }
+        if (u.mode == UNIT_FULL) prefetch_c_l2(P.epi, u, ew, lane, BN);
         const int buf = acc_it & 1;
         const uint32_t aph = (acc_it >> 1) & 1;
         ++acc_it;

@@ -11,7 +11,7 @@ import torch
 import quantized_gemm_tcgen05_gb300 as qg
 import oracle
 import synth
-from gpu_helpers import Lib, assert_close, op, run_grouped, run_problem
+from gpu_helpers import TORCH_DT, Lib, assert_close, dev_bits, op, run_grouped, run_problem
 
 pytestmark = pytest.mark.gpu
 
@@ -57,6 +57,43 @@ def test_schedules_and_pairs(lib, flags, kernel, monkeypatch):
                     alpha=1.0, beta=0.5)
     _check(lib, synth.with_epilogue(p, flags, seed=9, bias_type=synth.BF16), what=kernel)
     assert qg.gemm_last_choice(lib.h) == kernel
+
+
+def _padded(rows, cols, ld, dtype, fill=float("nan")):
+    """A [rows, cols] view with row stride ld (a multiple of 8 elements)."""
+    return torch.full((rows, ld), fill, dtype=dtype, device="cuda")[:, :cols]
+
+
+@pytest.mark.parametrize("kernel", ["umma_bn128/dp", "umma_bn128/splitk3", "umma_bn64/streamk", "umma2_bn256/dp",
+                                    "umma_bn64_swap/splitk2", "umma_bn16_swap/dp"])
+@pytest.mark.parametrize("d_type", [synth.BF16, synth.F16])
+def test_register_epilogue_forced(lib, kernel, d_type, monkeypatch):
+    # The register epilogue on every kernel shape (the TMA store switched
+    # off): 16-byte row pieces of C and D when the rows allow them, the
+    # swapped tile's transposed stores, the split-tile reductions, and the
+    # ragged last columns and rows; C is read (beta != 0) and D's rows are
+    # padded so that N is not a multiple of 8 while the rows stay aligned.
+    monkeypatch.setenv("GEMM_EPI_TMA", "0")
+    monkeypatch.setenv("GEMM_FORCE_KERNEL", kernel)
+    swap = "swap" in kernel
+    M, N, K = (40, 1001, 768) if swap else (200, 1001, 640)
+    a_type = synth.F16 if d_type == synth.F16 else synth.BF16
+    p = synth.dense(M, N, K, seed=40 + len(kernel), a_type=a_type, d_type=d_type, dist="normal", scale=0.05,
+                    alpha=1.25, beta=0.5)
+    p = synth.with_epilogue(p, BIAS | GELU, seed=11, bias_type=synth.F32)
+    ld = 1008
+    C = _padded(M, N, ld, TORCH_DT[d_type], 0.0)
+    C.copy_(dev_bits(p.C, p.c_type))
+    D = _padded(M, N, ld, TORCH_DT[d_type])
+    rc, D = run_problem(lib, p, D=D, C=C)
+    assert rc == 0, qg.gemm_status_string(rc)
+    assert qg.gemm_last_choice(lib.h) == kernel
+    ref, bound = oracle.gemm(p)
+    assert_close(D.double().cpu().numpy(), ref, bound, p.d_type, f"register epilogue {kernel}")
+    # and with unpadded rows of a multiple of 8 columns (no ragged piece)
+    p2 = synth.dense(M, 1000, K, seed=41, a_type=a_type, d_type=d_type, dist="normal", scale=0.05, alpha=1.0,
+                     beta=-0.75)
+    _check(lib, p2, what=f"register epilogue {kernel} N=1000")
 
 
 @pytest.mark.parametrize("flags", [BIAS | GELU, BIAS])
