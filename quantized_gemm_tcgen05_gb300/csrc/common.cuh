@@ -379,14 +379,42 @@ __device__ __forceinline__ void with_epi_act(const EpiParams& e, F&& f) {
     }
 }
 
+// The epilogue parameters the per-element arithmetic reads, copied into
+// registers once per chunk.  Read through the parameter block instead, they
+// would be re-read after every store of the chunk: the compiler cannot tell
+// that a store to shared or global memory leaves them unchanged, and the
+// re-reads made a chunk's conversion several times slower.
+struct EpiArith {
+    float alpha, beta;
+    int32_t relu, has_bias, bias_type;
+    const void* bias;
+    int64_t N;
+};
+
+__device__ __forceinline__ EpiArith epi_arith(const EpiParams& e) {
+    EpiArith a;
+    a.alpha = e.alpha;
+    a.beta = e.beta;
+    a.relu = (e.flags & EPI_RELU) != 0;
+    a.has_bias = (e.flags & EPI_BIAS) != 0;
+    a.bias_type = e.bias_type;
+    a.bias = e.bias;
+    a.N = e.N;
+    return a;
+}
+
+__device__ __forceinline__ float bias_at(const EpiArith& a, int64_t n) {
+    return (a.has_bias && n < a.N) ? ld_elem(a.bias, a.bias_type, n) : 0.0f;
+}
+
 // The value stored: alpha * acc + beta * c, then the fused steps of ACT with
 // the column's bias.
 template <int ACT>
-__device__ __forceinline__ float epi_value(const EpiParams& e, float acc, float c, float bias) {
+__device__ __forceinline__ float epi_value(const EpiArith& e, float acc, float c, float bias) {
     float x = e.beta != 0.0f ? fmaf(e.alpha, acc, e.beta * c) : e.alpha * acc;
     if constexpr (ACT >= 0) {
         x += bias;
-        if constexpr (ACT == 0) x = ((e.flags & EPI_RELU) && x < 0.0f) ? 0.0f : x;
+        if constexpr (ACT == 0) x = (e.relu && x < 0.0f) ? 0.0f : x;
         if constexpr (ACT == 2) x = 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
     }
     return x;
@@ -508,10 +536,12 @@ __device__ __forceinline__ void load_c_chunk(const EpiParams& e, const Unit& u, 
 // warp's private 32 x W fp32 buffer (swizzled by 16-byte quads) that turns the
 // row-per-thread TMEM layout into row-contiguous global stores.
 template <int W, int ACT, bool Q8>
-__device__ __forceinline__ void store_chunk_t(const EpiParams& e, const Unit& u, int ew, int lane, int col0,
+__device__ __forceinline__ void store_chunk_t(const EpiParams& ep, const Unit& u, int ew, int lane, int col0,
                                             const float (&v)[W], const CChunk<W>& cc, float4* staging) {
+    const EpiParams e = ep;  // in registers: the stores below would otherwise force re-reads of every field used
     constexpr int Q = W / 4;
     const int64_t boff_d = (int64_t)u.batch * e.d_bstride;
+    const EpiArith ar = epi_arith(e);
     if (e.swap) {
         // tile row -> output column n; tile column -> output row m.
         const int64_t nb = u.x_row0 + ew * 32;  // this warp's 32 output columns
@@ -521,10 +551,10 @@ __device__ __forceinline__ void store_chunk_t(const EpiParams& e, const Unit& u,
             // 32 columns) instead of one element per chunk column
             constexpr int PITCH = 40;  // halves per staged row: 80 bytes keeps the 16-byte reads spread over the banks
             uint16_t* t16 = reinterpret_cast<uint16_t*>(staging);
-            const float bn = ACT >= 0 ? bias_at(e, nb + lane) : 0.0f;
+            const float bn = ACT >= 0 ? bias_at(ar, nb + lane) : 0.0f;
 #pragma unroll
             for (int j = 0; j < W; ++j) {
-                const float x = epi_value<ACT>(e, v[j], cc.v[j], bn);
+                const float x = epi_value<ACT>(ar, v[j], cc.v[j], bn);
                 t16[j * PITCH + lane] = e.d_type == DT_F16 ? __half_as_ushort(__float2half_rn(x))
                                                            : __bfloat16_as_ushort(__float2bfloat16_rn(x));
             }
@@ -545,11 +575,11 @@ __device__ __forceinline__ void store_chunk_t(const EpiParams& e, const Unit& u,
         // store instruction is still row-contiguous
         const int64_t n = nb + lane;
         if (n >= e.N || ew * 32 + lane >= u.x_rows) return;
-        const float bn = ACT >= 0 ? bias_at(e, n) : 0.0f;
+        const float bn = ACT >= 0 ? bias_at(ar, n) : 0.0f;
 #pragma unroll
         for (int j = 0; j < W; ++j) {
             const int64_t m = u.y_row0 + col0 + j;
-            if (m < e.M) store_out<Q8>(e, boff_d + m * e.ldd + n, epi_value<ACT>(e, v[j], cc.v[j], bn), m);
+            if (m < e.M) store_out<Q8>(e, boff_d + m * e.ldd + n, epi_value<ACT>(ar, v[j], cc.v[j], bn), m);
         }
         return;
     }
@@ -574,7 +604,7 @@ __device__ __forceinline__ void store_chunk_t(const EpiParams& e, const Unit& u,
             float out[8];
 #pragma unroll
             for (int t = 0; t < 8; ++t)
-                out[t] = epi_value<ACT>(e, acc[t], cc.v[8 * it + t], ACT >= 0 ? bias_at(e, n0 + t) : 0.0f);
+                out[t] = epi_value<ACT>(ar, acc[t], cc.v[8 * it + t], ACT >= 0 ? bias_at(ar, n0 + t) : 0.0f);
             const int64_t di = boff_d + m * e.ldd + n0;
             if (n0 + 7 < e.N) {
                 if (elem_in_bounds(e, di, 8, e.d_extent)) st8(e.D, e.d_type, di, out);
@@ -591,7 +621,7 @@ __device__ __forceinline__ void store_chunk_t(const EpiParams& e, const Unit& u,
     if (ACT >= 0) {
         const int64_t nq = u.y_row0 + col0 + 4 * (lane % Q);
 #pragma unroll
-        for (int t = 0; t < 4; ++t) bq[t] = bias_at(e, nq + t);
+        for (int t = 0; t < 4; ++t) bq[t] = bias_at(ar, nq + t);
     }
 #pragma unroll
     for (int it = 0; it < Q; ++it) {
@@ -603,10 +633,10 @@ __device__ __forceinline__ void store_chunk_t(const EpiParams& e, const Unit& u,
         const int64_t n0 = u.y_row0 + col0 + 4 * j;
         if (rt >= u.x_rows || m >= e.M || n0 >= e.N) continue;
         const int64_t di = boff_d + m * e.ldd + n0;
-        const float4 o = make_float4(epi_value<ACT>(e, a.x, cc.v[4 * it], bq[0]),
-                                     epi_value<ACT>(e, a.y, cc.v[4 * it + 1], bq[1]),
-                                     epi_value<ACT>(e, a.z, cc.v[4 * it + 2], bq[2]),
-                                     epi_value<ACT>(e, a.w, cc.v[4 * it + 3], bq[3]));
+        const float4 o = make_float4(epi_value<ACT>(ar, a.x, cc.v[4 * it], bq[0]),
+                                     epi_value<ACT>(ar, a.y, cc.v[4 * it + 1], bq[1]),
+                                     epi_value<ACT>(ar, a.z, cc.v[4 * it + 2], bq[2]),
+                                     epi_value<ACT>(ar, a.w, cc.v[4 * it + 3], bq[3]));
         if (e.vec_ok && n0 + 3 < e.N) {
             store_out4<Q8>(e, di, o, m);
         } else {
@@ -1000,22 +1030,23 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
             __syncwarp();
         }
         if (store) {
+            const EpiArith ar = epi_arith(e);
             if (f32) {
                 uint8_t* row = buf + lane * 128;
                 const int64_t n0 = slab_x(u, c);
                 auto put = [&](auto act) {
                     constexpr int F = decltype(act)::value;
                     // lane l holds the bias of the chunk's column l (W = 32 columns)
-                    const float bl = F >= 0 ? bias_at(e, n0 + lane) : 0.0f;
+                    const float bl = F >= 0 ? bias_at(ar, n0 + lane) : 0.0f;
                     auto bcol = [&](int col) { return F >= 0 ? __shfl_sync(0xffffffffu, bl, col) : 0.0f; };
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         float4* pp = reinterpret_cast<float4*>(row + ((q ^ (lane & 7)) << 4));
                         const float4 cv = use_c ? *pp : make_float4(0.f, 0.f, 0.f, 0.f);
-                        *pp = make_float4(epi_value<F>(e, v[4 * q], cv.x, bcol(4 * q)),
-                                          epi_value<F>(e, v[4 * q + 1], cv.y, bcol(4 * q + 1)),
-                                          epi_value<F>(e, v[4 * q + 2], cv.z, bcol(4 * q + 2)),
-                                          epi_value<F>(e, v[4 * q + 3], cv.w, bcol(4 * q + 3)));
+                        *pp = make_float4(epi_value<F>(ar, v[4 * q], cv.x, bcol(4 * q)),
+                                          epi_value<F>(ar, v[4 * q + 1], cv.y, bcol(4 * q + 1)),
+                                          epi_value<F>(ar, v[4 * q + 2], cv.z, bcol(4 * q + 2)),
+                                          epi_value<F>(ar, v[4 * q + 3], cv.w, bcol(4 * q + 3)));
                     }
                 };
                 with_epi_act(e, put);
@@ -1024,7 +1055,7 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
                 const int64_t n0 = slab_x(u, c);
                 auto put = [&](auto act) {
                     constexpr int F = decltype(act)::value;
-                    const float bl = F >= 0 ? bias_at(e, n0 + lane) : 0.0f;
+                    const float bl = F >= 0 ? bias_at(ar, n0 + lane) : 0.0f;
                     auto bcol = [&](int col) { return F >= 0 ? __shfl_sync(0xffffffffu, bl, col) : 0.0f; };
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -1044,8 +1075,8 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
                         uint32_t ow[4];
 #pragma unroll
                         for (int t = 0; t < 4; ++t) {
-                            const float a = epi_value<F>(e, v[8 * q + 2 * t], cv[2 * t], bcol(8 * q + 2 * t));
-                            const float b2 = epi_value<F>(e, v[8 * q + 2 * t + 1], cv[2 * t + 1], bcol(8 * q + 2 * t + 1));
+                            const float a = epi_value<F>(ar, v[8 * q + 2 * t], cv[2 * t], bcol(8 * q + 2 * t));
+                            const float b2 = epi_value<F>(ar, v[8 * q + 2 * t + 1], cv[2 * t + 1], bcol(8 * q + 2 * t + 1));
                             if (bf16) {
                                 __nv_bfloat162 h = __floats2bfloat162_rn(a, b2);
                                 ow[t] = *reinterpret_cast<uint32_t*>(&h);
