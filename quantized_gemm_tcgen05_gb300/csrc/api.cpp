@@ -536,9 +536,9 @@ int launch_choice(gemm_handle* h, const Problem& p, const Choice& c, const gemm_
                 ok16(p.D, p.ldd, p.d_bs) &&
                 (e.C == nullptr || ok16(p.C, p.ldc, p.c_bs)) && !(c.pair && es == 4);
         if (e.tma) {
-            // buffers per epilogue warp: 32 KB of epilogue shared memory (16 KB
-            // in the CTA-pair kernel) split over 4 warps
-            e.ncb = c.pair ? 2 : (es == 2 ? 4 : 2);
+            // buffers per epilogue warp: 32 KB of epilogue shared memory split
+            // over 4 warps
+            e.ncb = es == 2 ? 4 : 2;
             rc = make_map_cd(h, &maps.d, p.D, p.d_type, p.M, p.N, p.ldd, p.batches, p.d_bs);
             if (rc == GEMM_OK && e.C) rc = make_map_cd(h, &maps.c, p.C, p.d_type, p.M, p.N, p.ldc, p.batches, p.c_bs);
             if (rc != GEMM_OK) return rc;

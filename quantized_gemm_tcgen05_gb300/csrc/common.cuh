@@ -1121,6 +1121,15 @@ __device__ void epilogue_tma(const GemmKernelParams& P, const CUtensorMap* tmC, 
     uint32_t acc_it = 0;
     while (ok && next_unit(P, w, u, BN)) {
         if (e.flags) prefetch_bias(e, u.y_row0, BN, lane);
+        // this warp's C slabs of the unit into L2 while its accumulator is
+        // computed: the slab copies issued during the epilogue then find them
+        // there instead of each waiting on HBM
+        if (use_c && lane < NCH) {
+            if (P.x3d)
+                tma_prefetch_l2_3d(tmC, slab_x(u, lane), slab_y(u), u.batch);
+            else
+                tma_prefetch_l2_2d(tmC, slab_x(u, lane), slab_y(u));
+        }
         const int buf = acc_it & 1;
         const uint32_t aph = (acc_it >> 1) & 1;
         ++acc_it;

@@ -37,9 +37,12 @@ struct PairCfg {
     static constexpr uint32_t STAGE_BYTES = (A_BYTES + B_BYTES + 1023) / 1024 * 1024;
     static constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * BN);
     static constexpr int MAX_STAGES = 12;
-    // the epilogue keeps two C/D buffers per warp (16-bit D; fp32 D uses the
-    // register path), leaving room for one more ring stage
-    static constexpr uint32_t EPI_BYTES = EPI_SMEM_BYTES / 2;
+    // the epilogue keeps four C/D buffers per warp (16-bit D; fp32 D uses the
+    // register path).  With stages of two K-steps the ring depth is the same
+    // as with two buffers at every tile width (3 stages at 224 and 256, 4 at
+    // 128), and the deeper C prefetch shortens the exposed epilogue of a
+    // program's last tile
+    static constexpr uint32_t EPI_BYTES = EPI_SMEM_BYTES;
     static constexpr uint32_t AUX_BYTES = (2 * MAX_STAGES + 7 + FIX_BARS + EPI_CBARS) * 8 + 16;
     static constexpr uint32_t FIXED_BYTES = 1024 + EPI_BYTES + AUX_BYTES;
     // a stage holds ks 64-wide K-steps of both operands
